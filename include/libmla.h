@@ -1,0 +1,218 @@
+/*
+ * libmla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) decode over
+ * a paged latent KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The two operations follow the interface on the FlashMLA-PyTorch page
+ * (flash_mla_interface.py: get_mla_metadata and flash_mla_with_kvcache) and
+ * the vLLM page "vllm.attention.ops.flashmla" (same functions, parameter
+ * and return tables):
+ *
+ *   mla_get_metadata  -- split-KV load-balancing schedule over the SMs
+ *                        (get_mla_metadata: tile_scheduler_metadata of shape
+ *                        (num_sm_parts, TileSchedulerMetaDataSize) and
+ *                        num_splits of shape (batch_size + 1), both int32)
+ *   mla_decode_fwd    -- the decode (flash_mla_with_kvcache / fwd_kvcache_mla):
+ *                        out (batch, s_q, h_q, head_dim_v) and the fp32
+ *                        softmax_lse (batch, h_q, s_q)
+ *
+ * Conventions shared by every call
+ *   - Every tensor argument is a plain device pointer owned by the caller;
+ *     libmla keeps no reference to it after the call returns.  Nothing is
+ *     allocated by libmla on any call.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and runs asynchronously; no call synchronizes the host
+ *     except mla_check_device_error.
+ *   - Every call returns an int status (MLA_OK or one of MLA_ERR_*); the
+ *     detail of the last failure on the calling thread is available from
+ *     mla_last_error().  A failing call enqueues nothing.
+ *   - Layouts use element strides; the last dimension of every tensor must
+ *     be contiguous.  bf16 tensors are IEEE bfloat16 bit patterns.
+ *
+ * The workspace convention (query the size, then pass caller-owned scratch)
+ * mirrors the two-phase C API on the Ascend ATB "MLA" page
+ * (AtbMLAGetWorkspaceSize, then AtbMLA).
+ */
+#ifndef LIBMLA_H
+#define LIBMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mla_stream_t; /* same handle as cudaStream_t */
+
+/* Status codes. */
+enum {
+    MLA_OK = 0,
+    MLA_ERR_ARG = 1,         /* invalid argument: shape, stride, alignment or NULL pointer   */
+    MLA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (see each call)  */
+    MLA_ERR_ARCH = 3,        /* current device is not compute capability 10.3 (sm_103)       */
+    MLA_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed                          */
+    MLA_ERR_WORKSPACE = 5,   /* workspace pointer NULL or smaller than mla_workspace_size     */
+    MLA_ERR_DEVICE = 6       /* a kernel reported an error (see mla_check_device_error)       */
+};
+
+/* Device-side error bits, reported by mla_check_device_error. */
+enum {
+    MLA_DEVERR_TIMEOUT = 1,     /* a bounded wait inside a kernel gave up; outputs are invalid */
+    MLA_DEVERR_BAD_BLOCK = 2    /* a needed block_table entry was outside [0, num_blocks)       */
+};
+
+/* int32 entries per tile_scheduler_metadata row (TileSchedulerMetaDataSize). */
+#define MLA_METADATA_SIZE 8
+
+/* Fixed dimensions of the MLA decode this library implements. */
+#define MLA_HEAD_DIM 576        /* 512 latent + 64 RoPE dims of q and of each cache row */
+#define MLA_HEAD_DIM_V 512      /* V = the first 512 dims of each cache row             */
+#define MLA_PAGE_BLOCK_SIZE 64  /* cache rows per physical block                        */
+
+/*
+ * Problem description for mla_decode_fwd / mla_workspace_size.
+ *
+ *   q            (batch, s_q, h_q, head_dim) bf16;        q_stride   = {batch, token, head}
+ *   k_cache      (num_blocks, page_block_size, h_k, head_dim) bf16;
+ *                                                          k_stride   = {block, row, kv-head}
+ *   block_table  (batch, max_blocks_per_seq) int32;        bt_stride  = elements per row
+ *   out          (batch, s_q, h_q, head_dim_v) bf16;       out_stride = {batch, token, head}
+ *   softmax_lse  (batch, h_q, s_q) fp32, contiguous.
+ *
+ * Requirements (else MLA_ERR_ARG): batch >= 0, s_q >= 1, h_k >= 1,
+ * h_q % h_k == 0, head_dim == 576, head_dim_v == 512, page_block_size == 64,
+ * num_blocks >= 1, max_blocks_per_seq >= 1, num_sm_parts >= 1; every stride a
+ * multiple of 8 elements and every bf16 base pointer 16-byte aligned.
+ * Limit (else MLA_ERR_UNSUPPORTED): s_q * h_q / h_k <= 1024 query rows per
+ * KV head.
+ */
+typedef struct {
+    int32_t batch;
+    int32_t s_q;
+    int32_t h_q;
+    int32_t h_k;
+    int32_t head_dim;
+    int32_t head_dim_v;
+    int32_t page_block_size;
+    int32_t num_blocks;
+    int32_t max_blocks_per_seq;
+    int32_t num_sm_parts;      /* rows of tile_scheduler_metadata */
+    int64_t q_stride[3];
+    int64_t k_stride[3];
+    int64_t bt_stride;
+    int64_t out_stride[3];
+} mla_shape_t;
+
+/*
+ * Number of scheduler parts (rows of tile_scheduler_metadata) that fill
+ * `device` for the given head configuration: the number of two-CTA clusters
+ * of the decode kernel that can be resident at once, divided by the number
+ * of 128-row blocks per KV head and by num_heads_k (at least 1).
+ * num_heads_per_head_k = s_q * h_q / h_k (vLLM page, get_mla_metadata
+ * parameter table).  Errors: MLA_ERR_ARG (non-positive argument),
+ * MLA_ERR_ARCH, MLA_ERR_CUDA.
+ */
+int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, int *num_sm_parts);
+
+/*
+ * Split-KV schedule (get_mla_metadata).  Reads cache_seqlens (device, int32,
+ * `batch` entries) on the device and writes
+ *   tile_scheduler_metadata  (num_sm_parts, MLA_METADATA_SIZE) int32, device
+ *   num_splits               (batch + 1) int32, device: exclusive prefix sum
+ *                            of the number of parts each sequence is split over
+ * Record of part p: [begin_b, begin_blk, end_b, end_blk, first_slot,
+ * num_blocks, 0, 0]; the part processes, for b in [begin_b, end_b], blocks
+ * [b == begin_b ? begin_blk : 0, b == end_b ? end_blk : ceil(L_b / 64)).
+ * Policy: greedy contiguous walk over (sequence, block) with a fixed cost of
+ * 4 blocks per segment and a per-part target of
+ * ceil((W + (num_sm_parts - 1) * 4) / num_sm_parts), W = sum(n_b + 4).
+ * Errors: MLA_ERR_ARG (NULL pointer, batch < 0, num_sm_parts < 1,
+ * num_heads_per_head_k < 1, num_heads_k < 1), MLA_ERR_UNSUPPORTED
+ * (batch > 16384), MLA_ERR_CUDA.
+ */
+int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k,
+                     int num_heads_k, int num_sm_parts, int32_t *tile_scheduler_metadata,
+                     int32_t *num_splits, mla_stream_t stream);
+
+/*
+ * Bytes of workspace mla_decode_fwd needs for `shape`: fp32 partial outputs
+ * and log-sum-exps of the sequences the schedule splits, for up to
+ * batch + num_sm_parts splits.  Errors: MLA_ERR_ARG.
+ */
+int mla_workspace_size(const mla_shape_t *shape, size_t *bytes);
+
+/*
+ * Paged MLA decode (flash_mla_with_kvcache / fwd_kvcache_mla).  For every
+ * sequence b, query token i < s_q and head h, with hk = h / (h_q / h_k),
+ * L = cache_seqlens[b] and n = causal ? L - s_q + 1 + i : L (clamped to
+ * [0, L]; bottom-right alignment):
+ *   s_t = softmax_scale * q[b,i,h,:] . k[t, hk, :]       t < n, all 576 dims
+ *   out[b,i,h,:]      = sum_t softmax(s)_t * k[t, hk, 0:512]   (V aliases K)
+ *   softmax_lse[b,h,i] = ln sum_t exp(s_t)
+ * where k[t] is row t % 64 of physical block block_table[b][t / 64].
+ * Rows with n == 0 get out = 0 and softmax_lse = -inf.
+ * softmax_scale <= 0 or NaN selects the default 1/sqrt(head_dim) (the
+ * interface's default of q.shape[-1] ** -0.5).
+ *
+ * tile_scheduler_metadata / num_splits must come from mla_get_metadata on
+ * the same cache_seqlens and num_sm_parts (not checked).  block_table
+ * entries past ceil(L / 64) are never read; needed entries outside
+ * [0, num_blocks) are not dereferenced and raise MLA_DEVERR_BAD_BLOCK.
+ * workspace: device scratch of at least mla_workspace_size bytes, 256-byte
+ * aligned, not used concurrently by another call.
+ * Errors: MLA_ERR_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_ARCH, MLA_ERR_WORKSPACE,
+ * MLA_ERR_CUDA.  Launches two kernels: mla_decode_splitkv then
+ * mla_decode_combine, with the same arguments.
+ */
+int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
+                   const int32_t *block_table, const int32_t *cache_seqlens,
+                   const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                   float softmax_scale, int causal, void *out, float *softmax_lse,
+                   void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * The first of the two launches of mla_decode_fwd: the persistent split-KV
+ * decode.  Sequences the schedule does not split are finished here (out and
+ * softmax_lse written); split ones leave fp32 partials in the workspace.
+ */
+int mla_decode_splitkv(const mla_shape_t *shape, const void *q, const void *k_cache,
+                       const int32_t *block_table, const int32_t *cache_seqlens,
+                       const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                       float softmax_scale, int causal, void *out, float *softmax_lse,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * The second launch of mla_decode_fwd: merges the partials of every split
+ * sequence by log-sum-exp weighting (lse = ln sum_s exp(lse_s),
+ * out = sum_s exp(lse_s - lse) * out_s) and writes out / softmax_lse for
+ * them, and out = 0, softmax_lse = -inf for empty sequences.
+ * Same arguments as mla_decode_fwd (q, k_cache and block_table unused).
+ */
+int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_cache,
+                       const int32_t *block_table, const int32_t *cache_seqlens,
+                       const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                       float softmax_scale, int causal, void *out, float *softmax_lse,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * Synchronizes the current device, then stores in *bits the OR of the
+ * MLA_DEVERR_* bits kernels of this library raised on it since the last
+ * clear, and clears them when `clear` is non-zero.  Returns MLA_OK, or
+ * MLA_ERR_CUDA when synchronization itself failed.
+ */
+int mla_check_device_error(int *bits, int clear);
+
+/* Static description of a status code. */
+const char *mla_status_string(int status);
+
+/* Detail message of the last failing call on the calling thread ("" if none). */
+const char *mla_last_error(void);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMLA_H */

@@ -1,0 +1,417 @@
+// api.cu -- the C ABI of libmla (declared in include/libmla.h): argument
+// validation, TMA descriptor encoding, and the kernel launches.
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "libmla.h"
+#include "decode_common.cuh"
+
+namespace mla {
+__global__ void mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
+                                   const __grid_constant__ DecodeParams p);
+__global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
+__global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
+uint32_t splitkv_smem_bytes();
+}  // namespace mla
+
+// Error bits raised by the kernels on this device (MLA_DEVERR_*).
+__device__ int g_mla_device_error = 0;
+
+namespace {
+
+using namespace mla;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxBatchMetadata = 16384;
+constexpr int kMaxRowsPerHead = 1024;
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceState {
+    bool ready = false;
+    int status = MLA_OK;
+    int sm_count = 0;
+    int max_clusters = 0;
+    int *err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device one-time setup (with that device current): architecture check,
+// kernel attributes, occupancy of the cluster kernel, device error word.
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3) {
+            st.ready = true;
+            st.status = MLA_ERR_ARCH;
+        } else {
+            const int smem = (int)splitkv_smem_bytes();
+            if ((e = cudaFuncSetAttribute(mla_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+                cudaSuccess)
+                return cuda_fail(e, "cudaFuncSetAttribute(splitkv)");
+            if ((e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          2 * kMaxBatchMetadata * 4)) != cudaSuccess)
+                return cuda_fail(e, "cudaFuncSetAttribute(metadata)");
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * 64, 1, 1);
+            cfg.blockDim = dim3(192, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, (void *)mla_splitkv_kernel, &cfg);
+            if (e != cudaSuccess || clusters <= 0) {
+                (void)cudaGetLastError();
+                clusters = st.sm_count / 2;
+            }
+            st.max_clusters = clusters;
+            void *addr = nullptr;
+            if ((e = cudaGetSymbolAddress(&addr, g_mla_device_error)) != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+            st.err_word = static_cast<int *>(addr);
+            st.ready = true;
+            st.status = MLA_OK;
+        }
+    }
+    if (st.status != MLA_OK)
+        return fail(st.status, "device %d is not compute capability 10.3 (sm_103)", dev);
+    *out = &st;
+    return MLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors over k_cache, cached per (pointer, geometry)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapEntry {
+    const void *ptr = nullptr;
+    int device = -1, num_blocks = 0, h_k = 0;
+    int64_t s0 = 0, s1 = 0, s2 = 0;
+    CUtensorMap m128, m64;
+    bool valid = false;
+};
+constexpr int kMapCache = 16;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+int get_encoder(EncodeTiledFn *fn) {
+    static EncodeTiledFn cached = nullptr;
+    if (!cached) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+            return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        cached = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    *fn = cached;
+    return MLA_OK;
+}
+
+int kcache_maps(const mla_shape_t *sh, const void *k_cache, CUtensorMap *m128, CUtensorMap *m64) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto &e : g_maps) {
+        if (e.valid && e.ptr == k_cache && e.device == dev && e.num_blocks == sh->num_blocks && e.h_k == sh->h_k &&
+            e.s0 == sh->k_stride[0] && e.s1 == sh->k_stride[1] && e.s2 == sh->k_stride[2]) {
+            *m128 = e.m128;
+            *m64 = e.m64;
+            return MLA_OK;
+        }
+    }
+    EncodeTiledFn enc;
+    int st = get_encoder(&enc);
+    if (st != MLA_OK) return st;
+    // dims (innermost first): head dim, kv head, row in block, block
+    const cuuint64_t gdim[4] = {(cuuint64_t)sh->head_dim, (cuuint64_t)sh->h_k, (cuuint64_t)sh->page_block_size,
+                                (cuuint64_t)sh->num_blocks};
+    const cuuint64_t gstr[3] = {(cuuint64_t)sh->k_stride[2] * 2, (cuuint64_t)sh->k_stride[1] * 2,
+                                (cuuint64_t)sh->k_stride[0] * 2};
+    const cuuint32_t box128[4] = {64, 1, 64, 1}, box64[4] = {32, 1, 64, 1}, es[4] = {1, 1, 1, 1};
+    MapEntry &e = g_maps[g_map_next];
+    CUresult r1 = enc(&e.m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k_cache), gdim, gstr, box128,
+                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r2 = enc(&e.m64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k_cache), gdim, gstr, box64,
+                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
+        e.valid = false;
+        return fail(MLA_ERR_ARG, "k_cache tensor map rejected by the driver (codes %d, %d): check alignment/strides",
+                    (int)r1, (int)r2);
+    }
+    e.ptr = k_cache; e.device = dev; e.num_blocks = sh->num_blocks; e.h_k = sh->h_k;
+    e.s0 = sh->k_stride[0]; e.s1 = sh->k_stride[1]; e.s2 = sh->k_stride[2];
+    e.valid = true;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    *m128 = e.m128;
+    *m64 = e.m64;
+    return MLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const mla_shape_t *sh) {
+    if (!sh) return fail(MLA_ERR_ARG, "shape is NULL");
+    if (sh->batch < 0) return fail(MLA_ERR_ARG, "batch %d < 0", sh->batch);
+    if (sh->s_q < 1 || sh->h_q < 1 || sh->h_k < 1)
+        return fail(MLA_ERR_ARG, "s_q, h_q, h_k must be >= 1 (got %d, %d, %d)", sh->s_q, sh->h_q, sh->h_k);
+    if (sh->h_q % sh->h_k != 0) return fail(MLA_ERR_ARG, "h_q %d not divisible by h_k %d", sh->h_q, sh->h_k);
+    if (sh->head_dim != MLA_HEAD_DIM) return fail(MLA_ERR_ARG, "head_dim must be 576 (got %d)", sh->head_dim);
+    if (sh->head_dim_v != MLA_HEAD_DIM_V)
+        return fail(MLA_ERR_ARG, "head_dim_v must be 512 (got %d)", sh->head_dim_v);
+    if (sh->page_block_size != MLA_PAGE_BLOCK_SIZE)
+        return fail(MLA_ERR_ARG, "page_block_size must be 64 (got %d)", sh->page_block_size);
+    if (sh->num_blocks < 1 || sh->max_blocks_per_seq < 1)
+        return fail(MLA_ERR_ARG, "num_blocks and max_blocks_per_seq must be >= 1");
+    if (sh->num_sm_parts < 1) return fail(MLA_ERR_ARG, "num_sm_parts must be >= 1");
+    const long long rows = (long long)sh->s_q * sh->h_q / sh->h_k;
+    if (rows > kMaxRowsPerHead)
+        return fail(MLA_ERR_UNSUPPORTED, "s_q*h_q/h_k = %lld query rows per KV head exceeds %d", rows, kMaxRowsPerHead);
+    for (int i = 0; i < 3; ++i) {
+        if (sh->q_stride[i] <= 0 || sh->q_stride[i] % 8 || sh->k_stride[i] <= 0 || sh->k_stride[i] % 8 ||
+            sh->out_stride[i] <= 0 || sh->out_stride[i] % 8)
+            return fail(MLA_ERR_ARG, "strides must be positive multiples of 8 elements");
+    }
+    if (sh->bt_stride < sh->max_blocks_per_seq) return fail(MLA_ERR_ARG, "bt_stride < max_blocks_per_seq");
+    return MLA_OK;
+}
+
+size_t workspace_bytes_for(const mla_shape_t *sh, size_t *lse_off) {
+    const size_t slots = (size_t)sh->batch + (size_t)sh->num_sm_parts;
+    const size_t rows = (size_t)sh->s_q * sh->h_q;        // h_k * R
+    const size_t o_bytes = slots * rows * MLA_HEAD_DIM_V * sizeof(float);
+    const size_t off = (o_bytes + 255) & ~(size_t)255;
+    if (lse_off) *lse_off = off;
+    return off + ((slots * rows * sizeof(float) + 255) & ~(size_t)255);
+}
+
+struct Prepared {
+    DecodeParams p;
+    dim3 grid;
+};
+
+int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int32_t *block_table,
+            const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale, int causal,
+            void *out, float *lse, void *ws, size_t ws_bytes, bool need_kv, Prepared *pr, DeviceState **dst) {
+    int st = check_shape(sh);
+    if (st != MLA_OK) return st;
+    if (!cache_seqlens || !md || !num_splits || !out || !lse)
+        return fail(MLA_ERR_ARG, "NULL tensor pointer");
+    if (need_kv && (!q || !k_cache || !block_table)) return fail(MLA_ERR_ARG, "NULL tensor pointer");
+    if ((need_kv && (!aligned16(q) || !aligned16(k_cache))) || !aligned16(out))
+        return fail(MLA_ERR_ARG, "q, k_cache and out must be 16-byte aligned");
+    size_t lse_off = 0;
+    const size_t need = workspace_bytes_for(sh, &lse_off);
+    if (!ws) return fail(MLA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MLA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (ws_bytes < need) return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+    st = device_state(dst);
+    if (st != MLA_OK) return st;
+
+    if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)sh->head_dim);
+    DecodeParams &p = pr->p;
+    memset(&p, 0, sizeof p);
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_s0 = sh->q_stride[0]; p.q_s1 = sh->q_stride[1]; p.q_s2 = sh->q_stride[2];
+    p.block_table = block_table;
+    p.bt_stride = sh->bt_stride;
+    p.seqlens = cache_seqlens;
+    p.md = md;
+    p.num_splits = num_splits;
+    p.out = static_cast<uint16_t *>(out);
+    p.o_s0 = sh->out_stride[0]; p.o_s1 = sh->out_stride[1]; p.o_s2 = sh->out_stride[2];
+    p.lse = lse;
+    p.ws_o = static_cast<float *>(ws);
+    p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + lse_off);
+    p.err = (*dst)->err_word;
+    p.batch = sh->batch; p.s_q = sh->s_q; p.h_q = sh->h_q; p.h_k = sh->h_k;
+    p.hpk = sh->h_q / sh->h_k;
+    p.rows = sh->s_q * p.hpk;
+    p.num_blocks = sh->num_blocks;
+    p.max_blocks = sh->max_blocks_per_seq;
+    p.num_parts = sh->num_sm_parts;
+    p.max_slots = sh->batch + sh->num_sm_parts;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const int row_blocks = (p.rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    pr->grid = dim3(2 * sh->num_sm_parts, row_blocks, sh->h_k);
+    return MLA_OK;
+}
+
+int launch_splitkv(const mla_shape_t *sh, const void *k_cache, const Prepared &pr, cudaStream_t stream) {
+    CUtensorMap m128, m64;
+    int st = kcache_maps(sh, k_cache, &m128, &m64);
+    if (st != MLA_OK) return st;
+    mla_splitkv_kernel<<<pr.grid, 192, splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
+    return MLA_OK;
+}
+
+int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t stream) {
+    const dim3 grid(sh->batch, sh->h_k, (pr.p.rows + 7) / 8);
+    mla_combine_kernel<<<grid, 256, 0, stream>>>(pr.p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char *mla_status_string(int status) {
+    switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_DEVICE: return "device-side error reported by a kernel";
+    default: return "unknown status";
+    }
+}
+
+const char *mla_last_error(void) { return t_last_error.c_str(); }
+
+int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, int *num_sm_parts) {
+    if (!num_sm_parts || num_heads_per_head_k < 1 || num_heads_k < 1)
+        return fail(MLA_ERR_ARG, "mla_get_num_sm_parts: bad argument");
+    int prev = 0;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device != prev && (e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    DeviceState *ds = nullptr;
+    int st = device_state(&ds);
+    if (device != prev) cudaSetDevice(prev);
+    if (st != MLA_OK) return st;
+    const int row_blocks = (num_heads_per_head_k + kRowsPerBlock - 1) / kRowsPerBlock;
+    int parts = ds->max_clusters / (row_blocks * num_heads_k);
+    *num_sm_parts = parts < 1 ? 1 : parts;
+    return MLA_OK;
+}
+
+int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k, int num_heads_k,
+                     int num_sm_parts, int32_t *tile_scheduler_metadata, int32_t *num_splits, mla_stream_t stream) {
+    if (!tile_scheduler_metadata || !num_splits || (batch > 0 && !cache_seqlens))
+        return fail(MLA_ERR_ARG, "mla_get_metadata: NULL pointer");
+    if (batch < 0 || num_sm_parts < 1 || num_heads_per_head_k < 1 || num_heads_k < 1)
+        return fail(MLA_ERR_ARG, "mla_get_metadata: bad argument");
+    if (batch > kMaxBatchMetadata) return fail(MLA_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatchMetadata);
+    DeviceState *ds = nullptr;
+    int st = device_state(&ds);
+    if (st != MLA_OK) return st;
+    const size_t smem = (size_t)2 * (batch > 0 ? batch : 1) * sizeof(int32_t);
+    mla_metadata_kernel<<<1, 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+        cache_seqlens, batch, num_sm_parts, tile_scheduler_metadata, num_splits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "metadata launch");
+    return MLA_OK;
+}
+
+int mla_workspace_size(const mla_shape_t *shape, size_t *bytes) {
+    if (!bytes) return fail(MLA_ERR_ARG, "bytes is NULL");
+    int st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    *bytes = workspace_bytes_for(shape, nullptr);
+    return MLA_OK;
+}
+
+int mla_decode_splitkv(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+                       const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
+                       int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    Prepared pr;
+    DeviceState *ds = nullptr;
+    int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
+                     ws_bytes, true, &pr, &ds);
+    if (st != MLA_OK) return st;
+    if (shape->batch == 0) return MLA_OK;
+    return launch_splitkv(shape, k_cache, pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+                       const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
+                       int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    Prepared pr;
+    DeviceState *ds = nullptr;
+    int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
+                     ws_bytes, false, &pr, &ds);
+    if (st != MLA_OK) return st;
+    if (shape->batch == 0) return MLA_OK;
+    return launch_combine(shape, pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+                   const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
+                   int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    Prepared pr;
+    DeviceState *ds = nullptr;
+    int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
+                     ws_bytes, true, &pr, &ds);
+    if (st != MLA_OK) return st;
+    if (shape->batch == 0) return MLA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = launch_splitkv(shape, k_cache, pr, s);
+    if (st != MLA_OK) return st;
+    return launch_combine(shape, pr, s);
+}
+
+int mla_check_device_error(int *bits, int clear) {
+    if (!bits) return fail(MLA_ERR_ARG, "bits is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_mla_device_error, sizeof v)) != cudaSuccess)
+        return cuda_fail(e, "read device error word");
+    *bits = v;
+    if (clear && v) {
+        const int zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_mla_device_error, &zero, sizeof zero)) != cudaSuccess)
+            return cuda_fail(e, "clear device error word");
+    }
+    return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// decode_common.cuh -- parameters and schedule walk shared by the decode kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kPage = 64;          // cache rows per physical block
+constexpr int kDqk = 576;          // q / cache row dims (512 latent + 64 RoPE)
+constexpr int kDv = 512;           // V dims (prefix of each cache row)
+constexpr int kMdSize = 8;         // int32 per scheduler record
+constexpr int kFixedCost = 4;      // schedule: cost of opening a segment, in blocks
+constexpr int kRowsPerBlock = 128; // query rows per CTA (tcgen05 M)
+
+// Device-side error bits (mirror MLA_DEVERR_* of the public header).
+constexpr int kErrTimeout = 1;
+constexpr int kErrBadBlock = 2;
+
+struct DecodeParams {
+    const uint16_t *q;             // bf16 (B, s_q, h_q, 576)
+    int64_t q_s0, q_s1, q_s2;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    const int32_t *seqlens;
+    const int32_t *md;             // (num_parts, 8)
+    const int32_t *num_splits;     // (B + 1)
+    uint16_t *out;                 // bf16 (B, s_q, h_q, 512)
+    int64_t o_s0, o_s1, o_s2;
+    float *lse;                    // (B, h_q, s_q)
+    float *ws_o;                   // (slots, h_k, R, 512) fp32 partial outputs
+    float *ws_lse;                 // (slots, h_k, R) fp32 partial lse
+    int *err;                      // device error word
+    int batch, s_q, h_q, h_k, hpk, rows;   // rows = R = s_q * h_q / h_k
+    int num_blocks, max_blocks, num_parts, max_slots;
+    int causal;
+    float scale_log2;              // softmax_scale * log2(e)
+};
+
+// One contiguous run of blocks of one sequence assigned to a part.
+struct Segment {
+    int b, lo, hi, L, slot, nsplit;
+};
+
+// Walks a part's record exactly as the schedule defines it.  Every role of
+// a CTA runs its own copy and sees the same segments.
+struct SegmentWalk {
+    int b, b0, k0, b1, k1, first_slot;
+    bool first;
+
+    __device__ __forceinline__ void init(const int32_t *rec) {
+        b0 = rec[0]; k0 = rec[1]; b1 = rec[2]; k1 = rec[3]; first_slot = rec[4];
+        b = b0 < 0 ? 0 : b0;
+        first = true;
+    }
+    __device__ __forceinline__ bool next(const DecodeParams &p, Segment &s) {
+        while (b <= b1 && b < p.batch) {
+            const int cb = b++;
+            int L = __ldg(p.seqlens + cb);
+            L = L < 0 ? 0 : L;
+            int nb = (L + kPage - 1) / kPage;
+            if (nb > p.max_blocks) {          // block table shorter than the sequence
+                atomicOr(p.err, kErrBadBlock);
+                nb = p.max_blocks;
+                L = nb * kPage;
+            }
+            const int lo = cb == b0 ? k0 : 0;
+            int hi = cb == b1 ? k1 : nb;
+            hi = hi > nb ? nb : hi;
+            if (lo >= hi || lo < 0) continue;
+            s.b = cb; s.lo = lo; s.hi = hi; s.L = L;
+            const int ns0 = __ldg(p.num_splits + cb), ns1 = __ldg(p.num_splits + cb + 1);
+            s.slot = first ? first_slot : ns0;
+            s.nsplit = ns1 - ns0;
+            first = false;
+            return true;
+        }
+        return false;
+    }
+};
+
+// Page-by-page cursor over a part's segments (used to run ahead of the
+// consumer, e.g. for L2 prefetch).
+struct PageCursor {
+    SegmentWalk walk;
+    Segment s;
+    int blk;
+    bool valid;
+
+    __device__ __forceinline__ void init(const int32_t *rec, const DecodeParams &p) {
+        walk.init(rec);
+        valid = walk.next(p, s);
+        blk = valid ? s.lo : 0;
+    }
+    __device__ __forceinline__ void advance(const DecodeParams &p) {
+        if (!valid) return;
+        if (++blk >= s.hi) {
+            valid = walk.next(p, s);
+            blk = valid ? s.lo : 0;
+        }
+    }
+};
+
+}  // namespace mla

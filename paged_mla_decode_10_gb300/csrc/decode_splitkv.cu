@@ -1,0 +1,541 @@
+// decode_splitkv.cu -- persistent split-KV paged MLA decode for sm_103a.
+//
+// Computes, for the (sequence, block-range) segments the scheduler gave a
+// part, the attention of up to 128 query rows (s_q * h_q / h_k rows are
+// stacked as the tcgen05 M dimension) against the part's 64-row pages of the
+// latent cache (FlashMLA-PyTorch page, flash_mla_interface.py,
+// flash_mla_with_kvcache docstring: q (B, s_q, h_q, 576), k_cache
+// (num_blocks, 64, h_k, 576), V = the first 512 dims of the cache rows).
+//
+// Work split.  One part is processed by a cluster of two CTAs on two SMs.
+// CTA c owns the V dims [256c, 256c + 256) and, for the QK^T contraction,
+// the same 256 latent dims plus RoPE dims [512 + 32c, 512 + 32c + 32).  Each
+// CTA therefore streams a disjoint 288-dim half of every page from HBM (no
+// byte is read twice), computes a partial logit tile S_c = Q_c K_c^T on the
+// tensor core, and the two CTAs swap their partial tiles through distributed
+// shared memory.  S = S_0 + S_1 is then bitwise identical in both CTAs, both
+// run the same online softmax, and each accumulates its half of
+// O = softmax(S) V.  The fp32 O half (128 x 256) fills half of TMEM, which
+// leaves room for two logit buffers and the resident Q half.
+//
+// Per CTA:
+//   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
+//   smem  Q RoPE half (SW64) | NS-stage page ring (4 x SW128 + 1 x SW64 boxes,
+//         36,864 B per page half) | P double buffer (SW128) | S exchange
+//         double buffer (fp32) | mbarriers
+//   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
+//   warp  4    TMA producer (one lane): page gather through block_table
+//   warp  5    MMA issuer (one lane) + TMEM allocation
+//
+// Online softmax (log2 domain) with lazy rescaling: the running max is only
+// raised when a page's max exceeds it by more than 8 (a factor of 256), so
+// the O correction (TMEM read-modify-write) is rare after the first pages.
+//
+// Every wait is bounded; a timeout sets MLA_DEVERR_TIMEOUT, drains the copies
+// and MMAs in flight, frees TMEM and returns.
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <cstdint>
+#include <cmath>
+
+#include "sm103.cuh"
+#include "decode_common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kStages = 3;
+constexpr uint32_t kHalfBytes = 36864;          // one CTA's 288-dim half of a page
+constexpr uint32_t OFF_QR = 0;                  // 128 rows x 64 B, SW64
+constexpr uint32_t OFF_K = 8192;
+constexpr uint32_t OFF_P = OFF_K + kStages * kHalfBytes;
+constexpr uint32_t OFF_X = OFF_P + 2 * 16384;
+constexpr uint32_t OFF_BAR = OFF_X + 2 * 32768;
+constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
+constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
+
+// barrier indices
+constexpr int B_KFULL = 0;
+constexpr int B_KEMPTY = B_KFULL + kStages;
+constexpr int B_SFULL = B_KEMPTY + kStages;
+constexpr int B_SEMPTY = B_SFULL + 2;
+constexpr int B_PFULL = B_SEMPTY + 2;
+constexpr int B_PEMPTY = B_PFULL + 2;
+constexpr int B_XFULL = B_PEMPTY + 2;
+constexpr int B_XEMPTY = B_XFULL + 2;
+constexpr int B_PVDONE = B_XEMPTY + 2;
+constexpr int B_OFINAL = B_PVDONE + 1;
+constexpr int B_QREADY = B_OFINAL + 1;
+constexpr int B_DRAIN = B_QREADY + 1;
+constexpr int B_COUNT = B_DRAIN + 1;
+static_assert(B_COUNT <= 64, "barrier area");
+
+constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr long long kTimeoutCycles = 4000000000ll;
+
+struct Ctx {
+    uint32_t base;              // shared address of the aligned smem base
+    volatile int *abort_flag;
+    int *err;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const Ctx &c, int i) { return c.base + OFF_BAR + 8u * i; }
+
+__device__ __noinline__ void raise_timeout(const Ctx &c) {
+    *c.abort_flag = 1;
+    atomicOr(c.err, kErrTimeout);
+}
+
+// Bounded wait; false when it timed out or another role already aborted.
+__device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (*c.abort_flag) return false;
+        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
+    }
+    return true;
+}
+__device__ __forceinline__ bool wait_bar_cluster(const Ctx &c, uint32_t bar, uint32_t parity) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test_cluster(bar, parity)) {
+        if (*c.abort_flag) return false;
+        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
+    }
+    return true;
+}
+// Teardown wait: ignores the abort flag (drains what is in flight), still bounded.
+__device__ __forceinline__ void drain_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return; }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// TMA producer: gathers this CTA's half of every page of the part.
+// ----------------------------------------------------------------------------
+__device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtensorMap *km128,
+                              const CUtensorMap *km64, const int32_t *rec, int cta, int hk,
+                              uint64_t policy) {
+    SegmentWalk walk;
+    walk.init(rec);
+    Segment s;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        const int32_t *bt_row = p.block_table + (int64_t)s.b * p.bt_stride;
+        for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
+            const uint32_t st = it % kStages;
+            if (!wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u)) { ok = false; break; }
+            int phys = __ldg(bt_row + blk);
+            if (phys < 0 || phys >= p.num_blocks) {
+                atomicOr(p.err, kErrBadBlock);
+                phys = 0;
+            }
+            const uint32_t full = bar_addr(c, B_KFULL + st);
+            const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
+            mbar_arrive_expect_tx(full, kHalfBytes);
+            // tensor map dims: {576 dims, h_k heads, 64 rows, num_blocks}
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
+            tma_load_4d(dst + 32768u, km64, full, 512 + 32 * cta, hk, 0, phys, policy);
+        }
+    }
+    // Drain: every copy issued must have landed before the CTA may exit.
+    const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+    for (uint32_t j = first; j < it; ++j) drain_bar(c, bar_addr(c, B_KFULL + j % kStages), (j / kStages) & 1u);
+}
+
+// ----------------------------------------------------------------------------
+// MMA issuer.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i, bool first_of_seg, int lane) {
+    const uint32_t st = i % kStages, pb = i & 1u;
+    bool ok = wait_bar(c, bar_addr(c, B_PFULL + pb), (i >> 1) & 1u);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    tc_fence_after();
+    if (lane == 0) {
+        constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
+        const uint32_t pbase = c.base + OFF_P + pb * 16384u;
+        const uint32_t vbase = c.base + OFF_K + st * kHalfBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_sdesc(pbase + kk * 32u, 16, 1024, kSwizzle128B);
+            const uint64_t bd = make_sdesc(vbase + kk * 2048u, 8192, 1024, kSwizzle128B);
+            umma_ss(tmem + TM_O, ad, bd, idPV, (first_of_seg && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(bar_addr(c, B_KEMPTY + st));
+        umma_commit(bar_addr(c, B_PEMPTY + pb));
+        umma_commit(bar_addr(c, B_PVDONE));
+    }
+    __syncwarp();
+    return true;
+}
+
+__device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem, int lane) {
+    SegmentWalk walk;
+    walk.init(rec);
+    Segment s;
+    uint32_t it = 0, g = 0;
+    bool ok = true;
+    constexpr uint32_t idS = make_idesc_bf16(128, 64, false, false);
+    while (ok && walk.next(p, s)) {
+        ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_QREADY), g & 1u));
+        if (!ok) break;
+        tc_fence_after();
+        const int nb_seq = (s.L + kPage - 1) / kPage;
+        const int tail = s.L & (kPage - 1);
+        const int n = s.hi - s.lo;
+        for (int j = 0; j < n; ++j, ++it) {
+            const uint32_t st = it % kStages, sb = it & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (it / kStages) & 1u));
+            if (!ok) break;
+            const uint32_t stage = c.base + OFF_K + st * kHalfBytes;
+            if (s.lo + j == nb_seq - 1 && tail != 0) {
+                // Rows past the sequence end may hold anything (even NaN); the
+                // P.V product would turn 0 * NaN into NaN, so zero them here.
+                uint8_t *gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(stage));
+                const int rows = kPage - tail;
+                for (int idx = lane; idx < rows * 36; idx += 32) {
+                    const int r = tail + idx / 36, ch = idx % 36;
+                    uint8_t *dst = ch < 32 ? gen + (ch >> 3) * 8192 + r * 128 + (ch & 7) * 16
+                                           : gen + 32768 + r * 64 + (ch - 32) * 16;
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SEMPTY + sb), ((it >> 1) & 1u) ^ 1u));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t dS = tmem + TM_S + 64u * sb;
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t bd = make_sdesc(stage + (kk >> 2) * 8192u + (kk & 3) * 32u, 16, 1024, kSwizzle128B);
+                    umma_ts(dS, tmem + TM_Q + 8u * kk, bd, idS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ad = make_sdesc(c.base + OFF_QR + kk * 32u, 16, 512, kSwizzle64B);
+                    const uint64_t bd = make_sdesc(stage + 32768u + kk * 32u, 16, 512, kSwizzle64B);
+                    umma_ss(dS, ad, bd, idS, 1u);
+                }
+                umma_commit(bar_addr(c, B_SFULL + sb));
+            }
+            __syncwarp();
+            if (j > 0) {
+                if (!issue_pv(c, tmem, it - 1, j == 1, lane)) { ok = false; break; }
+            }
+        }
+        if (!ok) break;
+        if (!issue_pv(c, tmem, it - 1, n == 1, lane)) { ok = false; break; }
+        if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
+        __syncwarp();
+        ++g;
+    }
+    // Drain: every MMA issued must complete before TMEM is freed.
+    if (lane == 0) umma_commit(bar_addr(c, B_DRAIN));
+    __syncwarp();
+    drain_bar(c, bar_addr(c, B_DRAIN), 0);
+}
+
+// ----------------------------------------------------------------------------
+// Softmax / epilogue warps (thread r owns query row r of the 128-row block).
+// ----------------------------------------------------------------------------
+__device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem,
+                             int cta, int rb, int hk) {
+    const int r = threadIdx.x;                 // 0..127
+    const int warp = r >> 5;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int row_g = rb * kRowsPerBlock + r;  // row within the KV head's R rows
+    const bool row_real = row_g < p.rows;
+    const bool warp_active = rb * kRowsPerBlock + warp * 32 < p.rows;
+    const int qi = row_g / p.hpk;              // query token i
+    const int qh = hk * p.hpk + row_g % p.hpk; // query head h
+    const uint32_t peer = (uint32_t)(cta ^ 1);
+
+    // shared addresses
+    const uint32_t xrow_local[2] = {c.base + OFF_X + r * 256u, c.base + OFF_X + 32768u + r * 256u};
+    uint32_t xrow_peer[2], xfull_peer[2], xempty_peer[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        xrow_peer[k] = mapa_shared(xrow_local[k], peer);
+        xfull_peer[k] = mapa_shared(bar_addr(c, B_XFULL + k), peer);
+        xempty_peer[k] = mapa_shared(bar_addr(c, B_XEMPTY + k), peer);
+    }
+    uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
+
+    SegmentWalk walk;
+    walk.init(rec);
+    Segment s;
+    uint32_t it = 0, g = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        // ---- Q half -> TMEM (latent dims, bf16 pairs) and smem (RoPE dims, SW64)
+        {
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(
+                p.q + (int64_t)s.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t w[64];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    uint4 x = row_real ? __ldg(qrow + cta * 32 + half * 16 + v) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+                }
+                tmem_st_32x32b_x64(tmem + lane_base + TM_Q + 64u * half, w);
+            }
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint4 x = row_real ? __ldg(qrow + 64 + cta * 4 + ch) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz64_offset(r, ch)) = x;
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_addr(c, B_QREADY));
+        }
+        int n_vis = p.causal ? s.L - p.s_q + 1 + qi : s.L;
+        n_vis = n_vis < 0 ? 0 : (n_vis > s.L ? s.L : n_vis);
+        float m_ref = -INFINITY, l_sum = 0.f;
+
+        for (int blk = s.lo; blk < s.hi && ok; ++blk, ++it) {
+            const uint32_t sb = it & 1u, ph = (it >> 1) & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), ph));
+            if (!ok) break;
+            tc_fence_after();
+            float sv[64];
+            if (warp_active) {
+                uint32_t raw[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + TM_S + 64u * sb, raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(c, B_SEMPTY + sb));
+            if (!warp_active) {
+                mbar_arrive(bar_addr(c, B_PFULL + sb));
+                continue;
+            }
+            // ---- exchange partial logits with the peer CTA
+            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XEMPTY + sb), ph ^ 1u));
+            if (!ok) break;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint32_t a = xrow_peer[sb] + ((uint32_t)(ch ^ (r & 7)) << 4);
+                asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(a), "f"(sv[4 * ch]), "f"(sv[4 * ch + 1]), "f"(sv[4 * ch + 2]), "f"(sv[4 * ch + 3])
+                             : "memory");
+            }
+            mbar_arrive_remote(xfull_peer[sb]);
+            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XFULL + sb), ph));
+            if (!ok) break;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const float4 t = *reinterpret_cast<const float4 *>(
+                    smem_gen + (xrow_local[sb] - c.base) + ((ch ^ (r & 7)) << 4));
+                sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
+            }
+            mbar_arrive_remote(xempty_peer[sb]);
+
+            // ---- mask + scale (log2 domain) + page max
+            const int nv = n_vis - blk * kPage;   // visible keys of this row in this page
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                sv[j] = j < nv ? sv[j] * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[j]);
+            }
+            const bool o_live = m_ref != -INFINITY;
+            const bool raise = mt > m_ref + kRescaleThreshold;  // true for the first finite page
+            float factor = 1.f;
+            if (raise) {
+                if (o_live) factor = ex2_approx(m_ref - mt);
+                m_ref = mt;
+                l_sum *= factor;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t pk[32];
+            float psum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = ex2_approx(sv[2 * j] - m_use), p1 = ex2_approx(sv[2 * j + 1] - m_use);
+                pk[j] = pack_bf16x2(p0, p1);
+                psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
+            }
+            l_sum += psum;
+            // ---- P row -> smem (K-major SW128), once PV(it - 2) released the buffer
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PEMPTY + sb), ph ^ 1u));
+            if (!ok) break;
+            uint8_t *prow = smem_gen + OFF_P + sb * 16384u;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(prow + swz128_offset(r, ch)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            // ---- lazy O correction, after PV(it - 1) has landed in TMEM
+            if (__any_sync(0xffffffffu, raise && o_live)) {
+                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PVDONE), (it - 1) & 1u));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t o[64];
+                    tmem_ld_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+                    tmem_st_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_addr(c, B_PFULL + sb));
+        }
+        if (!ok) break;
+
+        // ---- epilogue: normalise this CTA's O half and store
+        ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_OFINAL), g & 1u));
+        if (!ok) break;
+        tc_fence_after();
+        if (warp_active) {
+            const bool live = l_sum > 0.f;
+            const float inv = live ? 1.f / l_sum : 0.f;
+            float lse_nat = -INFINITY;
+            if (live) {
+                float lg;
+                asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_sum));
+                lse_nat = (m_ref + lg) * 0.6931471805599453f;
+            }
+            const bool direct = s.nsplit == 1;
+            const bool slot_ok = s.slot >= 0 && s.slot < p.max_slots;
+            if (!direct && !slot_ok && row_real) atomicOr(p.err, kErrBadBlock);
+            const int64_t prow_idx = ((int64_t)s.slot * p.h_k + hk) * p.rows + row_g;
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t o[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
+                tmem_ld_wait();
+                if (!row_real) continue;
+                if (direct) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        p.out + (int64_t)s.b * p.o_s0 + (int64_t)qi * p.o_s1 + (int64_t)qh * p.o_s2 + 256 * cta + 64 * q4);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                        dst[v] = w;
+                    }
+                } else if (slot_ok) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow_idx * kDv + 256 * cta + 64 * q4);
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+                }
+            }
+            if (row_real && cta == 0) {
+                if (direct) p.lse[((int64_t)s.b * p.h_q + qh) * p.s_q + qi] = lse_nat;
+                else if (slot_ok) p.ws_lse[prow_idx] = lse_nat;
+            }
+        }
+        tc_fence_before();
+        ++g;
+    }
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
+                   const __grid_constant__ DecodeParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Ctx c;
+    c.base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (c.base - raw);
+    c.abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    c.err = p.err;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = (int)cluster_ctarank();
+    const int part = blockIdx.x >> 1;
+    const int rb = blockIdx.y, hk = blockIdx.z;
+    const int32_t *rec = p.md + part * kMdSize;
+
+    const int rows_here = p.rows - rb * kRowsPerBlock;
+    const int nwa = rows_here >= 128 ? 4 : (rows_here + 31) / 32;   // softmax warps with real rows
+
+    if (threadIdx.x == 0) {
+        *c.abort_flag = 0;
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar_addr(c, B_KFULL + i), 1);
+            mbar_init(bar_addr(c, B_KEMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(c, B_SFULL + i), 1);
+            mbar_init(bar_addr(c, B_SEMPTY + i), 128);
+            mbar_init(bar_addr(c, B_PFULL + i), 128);
+            mbar_init(bar_addr(c, B_PEMPTY + i), 1);
+            mbar_init(bar_addr(c, B_XFULL + i), 32 * nwa);
+            mbar_init(bar_addr(c, B_XEMPTY + i), 32 * nwa);
+        }
+        mbar_init(bar_addr(c, B_PVDONE), 1);
+        mbar_init(bar_addr(c, B_OFINAL), 1);
+        mbar_init(bar_addr(c, B_QREADY), 128);
+        mbar_init(bar_addr(c, B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&km128);
+        tma_prefetch_desc(&km64);
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    // P buffers start at zero: rows of warps without real rows are never written.
+    for (uint32_t i = threadIdx.x; i < 2 * 16384 / 16; i += blockDim.x)
+        *reinterpret_cast<uint4 *>(smem + OFF_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_arrive();   // peer barriers are initialised before any remote arrive
+    cluster_wait();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        softmax_role(c, p, rec, tmem, cta, rb, hk);
+    } else if (warp == 4) {
+        if (lane == 0) {
+            const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+            producer_role(c, p, &km128, &km64, rec, cta, hk, pol);
+        }
+    } else {
+        mma_role(c, p, rec, tmem, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, 512);
+    cluster_arrive();   // no CTA leaves while its peer may still touch its shared memory
+    cluster_wait();
+}
+
+uint32_t splitkv_smem_bytes() { return kSmemBytes; }
+
+}  // namespace mla

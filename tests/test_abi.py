@@ -1,0 +1,90 @@
+"""The C-ABI library loads, exports every function include/libmla.h declares,
+and its host-side validation rejects bad arguments (CPU only: none of these
+calls reaches a kernel)."""
+import ctypes
+
+import pytest
+
+import __graft_entry__ as G
+
+
+@pytest.fixture(scope="module")
+def lib():
+    G._load_by_path("_libmla_build", "paged_mla_decode_10_gb300/build.py").build()
+    from paged_mla_decode_10_gb300 import _lib
+    return _lib.load()
+
+
+def test_exports_every_declared_function(lib):
+    from paged_mla_decode_10_gb300 import _lib
+    names = _lib.header_functions()
+    assert {"mla_get_metadata", "mla_decode_fwd", "mla_workspace_size", "mla_get_num_sm_parts",
+            "mla_check_device_error"} <= set(names)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.mla_status_string(code)
+    assert lib.mla_version() >= 100
+
+
+def _shape(**kw):
+    from paged_mla_decode_10_gb300._lib import MlaShape
+    sh = MlaShape()
+    vals = dict(batch=2, s_q=1, h_q=16, h_k=1, head_dim=576, head_dim_v=512, page_block_size=64,
+                num_blocks=8, max_blocks_per_seq=5, num_sm_parts=4)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(sh, k, v)
+    qs = kw.get("q_stride", (16 * 576, 16 * 576, 576))
+    ks = kw.get("k_stride", (64 * 576, 576, 576))
+    os_ = kw.get("out_stride", (16 * 512, 16 * 512, 512))
+    for i in range(3):
+        sh.q_stride[i], sh.k_stride[i], sh.out_stride[i] = qs[i], ks[i], os_[i]
+    sh.bt_stride = kw.get("bt_stride", 5)
+    return sh
+
+
+def test_workspace_size_formula(lib):
+    n = ctypes.c_size_t(0)
+    sh = _shape()
+    assert lib.mla_workspace_size(ctypes.byref(sh), ctypes.byref(n)) == 0
+    slots, rows = 2 + 4, 16
+    o = slots * rows * 512 * 4
+    o = (o + 255) // 256 * 256
+    l = (slots * rows * 4 + 255) // 256 * 256
+    assert n.value == o + l
+
+
+@pytest.mark.parametrize("bad", [
+    dict(head_dim=512), dict(head_dim_v=256), dict(page_block_size=32), dict(h_q=12, h_k=8),
+    dict(s_q=0), dict(num_sm_parts=0), dict(num_blocks=0), dict(q_stride=(16 * 576, 16 * 576, 577)),
+    dict(bt_stride=4), dict(batch=-1),
+])
+def test_workspace_size_rejects_bad_shapes(lib, bad):
+    n = ctypes.c_size_t(0)
+    sh = _shape(**bad)
+    assert lib.mla_workspace_size(ctypes.byref(sh), ctypes.byref(n)) == 1   # MLA_ERR_ARG
+    assert lib.mla_last_error()
+
+
+def test_too_many_rows_is_unsupported(lib):
+    n = ctypes.c_size_t(0)
+    sh = _shape(s_q=16, h_q=128)
+    assert lib.mla_workspace_size(ctypes.byref(sh), ctypes.byref(n)) == 2   # MLA_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_null_pointers_before_any_cuda_call(lib):
+    sh = _shape()
+    rc = lib.mla_decode_fwd(ctypes.byref(sh), None, None, None, None, None, None, ctypes.c_float(0.0), 0,
+                            None, None, None, 0, None)
+    assert rc == 1
+
+
+def test_metadata_rejects_bad_arguments(lib):
+    assert lib.mla_get_metadata(None, 4, 128, 1, 76, None, None, None) == 1
+    dummy = ctypes.c_void_p(256)
+    assert lib.mla_get_metadata(dummy, -1, 128, 1, 76, dummy, dummy, None) == 1
+    assert lib.mla_get_metadata(dummy, 4, 128, 1, 0, dummy, dummy, None) == 1

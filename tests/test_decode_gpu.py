@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: |out - ref| <= 1e-2 + 1e-2 |ref| element-wise (bf16 out) and
+|lse - ref| <= 2e-3; integer schedule outputs bit-exact against the policy
+restatement and valid under the coverage invariants.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import metadata as OM
+from tests.parity import assert_close, oracle, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _custom(name, batch, s_q, h_q, seqlens, h_k=1, causal=False, seed=1, q_std=1.0, poison=True):
+    w = workloads.Workload(name, batch=len(seqlens), s_q=s_q, h_q=h_q, h_k=h_k, causal=causal,
+                           seqlens=("fixed", tuple(seqlens)), q_std=q_std)
+    return workloads.make_inputs(w, seed=seed, poison=poison)
+
+
+def test_tiny_workload_all_rows():
+    inp = workloads.make_inputs("tiny")
+    out, lse, md, ns = run_gpu(inp)
+    ref_o, ref_l = oracle(inp)
+    assert_close(out, lse, ref_o, ref_l, where="tiny")
+
+
+@pytest.mark.parametrize("parts", [1, 3, 7, None])
+@pytest.mark.parametrize("case", [
+    ("h128_ragged", 1, 128, [1, 63, 64, 65, 200, 1000], 1, False),
+    ("h16_ragged", 1, 16, [5, 64, 129, 700], 1, False),
+    ("h64", 1, 64, [300, 17, 2000], 1, False),
+    ("mtp_causal_small", 2, 128, [2, 64, 65, 333, 1024], 1, True),
+    ("s3_causal", 3, 32, [3, 70, 640], 1, True),
+    ("gqa_hk2", 1, 32, [90, 513], 2, False),
+])
+def test_small_cases_multi_tile(case, parts):
+    name, s_q, h_q, Ls, h_k, causal = case
+    inp = _custom(name, len(Ls), s_q, h_q, Ls, h_k=h_k, causal=causal, seed=len(Ls) * 31 + h_q)
+    out, lse, md, ns = run_gpu(inp, num_sm_parts=parts)
+    ref_o, ref_l = oracle(inp)
+    assert_close(out, lse, ref_o, ref_l, where=f"{name} parts={parts}")
+
+
+def test_empty_and_invisible_rows():
+    # L = 0 sequence; causal L=1 with s_q=3 (rows i=0,1 see nothing)
+    inp = _custom("edge", 3, 3, 16, [0, 1, 130], causal=True, seed=4)
+    out, lse, md, ns = run_gpu(inp, num_sm_parts=2)
+    ref_o, ref_l = oracle(inp)
+    assert_close(out, lse, ref_o, ref_l, where="edge")
+    assert (out[0] == 0).all() and torch.isinf(lse[0]).all()
+
+
+def test_metadata_matches_policy_bit_exact():
+    import paged_mla_decode_10_gb300 as M
+    rng = np.random.default_rng(3)
+    cases = [([100, 257], 76), ([131072] + [1024] * 31, 76), (list(rng.integers(1, 8193, 64)), 76),
+             (list(rng.integers(0, 300, 37)), 5), ([0, 0, 0], 3), (list(rng.integers(2048, 16385, 256)), 76),
+             ([4096] * 128, 38), ([7], 200)]
+    for Ls, parts in cases:
+        L = torch.tensor([int(x) for x in Ls], dtype=torch.int32, device="cuda")
+        md, ns = M.mla_get_metadata(L, 128, 1, num_sm_parts=parts)
+        md_ref, ns_ref = OM.schedule([int(x) for x in Ls], parts)
+        np.testing.assert_array_equal(md.cpu().numpy(), md_ref)
+        np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
+        OM.check_metadata([int(x) for x in Ls], md.cpu().numpy(), ns.cpu().numpy())
+
+
+def test_num_sm_parts_variation_consistent():
+    inp = _custom("parts", 4, 1, 128, [3000, 100, 64, 2049], seed=9)
+    ref_o, ref_l = oracle(inp)
+    import paged_mla_decode_10_gb300 as M
+    default = M.mla_get_num_sm_parts(128, 1)
+    outs = []
+    for parts in (1, 7, default, 4 * default):
+        out, lse, _, _ = run_gpu(inp, num_sm_parts=parts)
+        assert_close(out, lse, ref_o, ref_l, where=f"parts={parts}")
+        outs.append(out.float())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() < 2e-2
+
+
+def test_page_permutation_invariance():
+    inp = workloads.make_inputs("tiny", seed=77)
+    out1, lse1, _, _ = run_gpu(inp)
+    g = torch.Generator().manual_seed(5)
+    perm = torch.randperm(inp.k_cache.shape[0], generator=g)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    bt2 = inp.block_table.clone()
+    m = bt2 >= 0
+    bt2[m] = inv[bt2[m].long()].to(torch.int32)
+    inp2 = workloads.Inputs(inp.workload, inp.q, inp.k_cache[perm].contiguous(), bt2, inp.cache_seqlens,
+                            inp.scale, inp.seed)
+    out2, lse2, _, _ = run_gpu(inp2)
+    # same schedule, same arithmetic order: identical results
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_peaked_softmax_small_case():
+    """Scale x8: sharper softmax, where a systematic error would not hide in the tolerance."""
+    inp = _custom("peaked", 3, 1, 128, [70, 600, 1500], seed=12)
+    scale = 8.0 / math.sqrt(576)
+    out, lse, _, _ = run_gpu(inp, scale=scale, num_sm_parts=5)
+    ref_o, ref_l = oracle(inp, scale=scale)
+    assert_close(out, lse, ref_o, ref_l, where="peaked")
+    rel = (out.float().cpu().numpy() - ref_o).std() / ref_o.std()
+    assert rel < 2e-2, rel
+
+
+def test_strided_inputs():
+    """q a slice of a wider tensor; k_cache blocks with padding between them."""
+    import paged_mla_decode_10_gb300 as M
+    inp = _custom("strided", 3, 2, 16, [77, 130, 9], causal=True, seed=21)
+    d = inp.to("cuda")
+    qbig = torch.zeros(3, 2, 24, 576, dtype=torch.bfloat16, device="cuda")
+    qbig[:, :, 4:20] = d.q
+    q = qbig[:, :, 4:20]
+    kbig = torch.zeros(d.k_cache.shape[0], 72, 1, 576, dtype=torch.bfloat16, device="cuda")
+    kbig[:, :64] = d.k_cache
+    k = kbig[:, :64]
+    md, ns = M.mla_get_metadata(d.cache_seqlens, inp.workload.rows, 1, num_sm_parts=3)
+    obig = torch.zeros(3, 2, 16, 640, dtype=torch.bfloat16, device="cuda")
+    out = obig[..., 64:576]
+    out, lse = M.mla_decode_fwd(q, k, d.block_table, d.cache_seqlens, 512, md, ns, inp.scale, True, out=out)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle(inp)
+    assert_close(out, lse, ref_o, ref_l, where="strided")
+    assert (obig[..., :64] == 0).all() and (obig[..., 576:] == 0).all()
+
+
+def test_bad_block_id_is_reported_not_faulting():
+    import paged_mla_decode_10_gb300 as M
+    M.mla_check_device_error(clear=True)
+    inp = _custom("badblk", 2, 1, 16, [100, 64], seed=3)
+    d = inp.to("cuda")
+    bt = d.block_table.clone()
+    bt[0, 1] = 10_000
+    md, ns = M.mla_get_metadata(d.cache_seqlens, 16, 1, num_sm_parts=2)
+    M.mla_decode_fwd(d.q, d.k_cache, bt, d.cache_seqlens, 512, md, ns, inp.scale, False)
+    bits = M.mla_check_device_error(clear=True)
+    assert bits & 2
+    assert M.mla_check_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "mtp_causal", "skewed_long", "lowhead_tp"])
+def test_full_size_workloads_sampled_rows(name):
+    """Full sizes, the launch configuration the benchmark times (default parts),
+    checked on sampled rows the oracle computes one by one."""
+    inp = workloads.make_inputs(name, device="cuda")
+    out, lse, md, ns = run_gpu(inp)
+    L = inp.cache_seqlens.cpu().tolist()
+    OM.check_metadata(L, md.cpu().numpy(), ns.cpu().numpy())
+    rows = sample_rows(inp, 24, seed=1)
+    ref_o, ref_l = oracle(inp, rows=rows)
+    assert_close(out, lse, ref_o, ref_l, rows=rows, where=name)
+    import paged_mla_decode_10_gb300 as M
+    assert M.mla_check_device_error(clear=True) == 0
