@@ -20,9 +20,10 @@
 //
 // Per CTA:
 //   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
-//   smem  Q RoPE half (SW64) | NS-stage page ring (4 x SW128 + 1 x SW64 boxes,
-//         36,864 B per page half) | P double buffer (SW128) | S exchange
-//         double buffer (fp32) | mbarriers
+//   smem  Q RoPE half (SW64) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
+//         36,864 B per page half) | S exchange double buffer (fp32) | mbarriers
+//   P (bf16) is written back over the S buffer it came from and read by the
+//   PV MMA straight from TMEM.
 //   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
 //   warp  4    TMA producer (one lane): page gather through block_table
 //   warp  5    MMA issuer (one lane) + TMEM allocation
@@ -45,26 +46,24 @@ namespace mla {
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
+constexpr int kPrefetchPages = 8;               // L2 prefetch distance of the producer
 constexpr uint32_t kHalfBytes = 36864;          // one CTA's 288-dim half of a page
 constexpr uint32_t OFF_QR = 0;                  // 128 rows x 64 B, SW64
 constexpr uint32_t OFF_K = 8192;
-constexpr uint32_t OFF_P = OFF_K + kStages * kHalfBytes;
-constexpr uint32_t OFF_X = OFF_P + 2 * 16384;
+constexpr uint32_t OFF_X = OFF_K + kStages * kHalfBytes;
 constexpr uint32_t OFF_BAR = OFF_X + 2 * 32768;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier indices
 constexpr int B_KFULL = 0;
 constexpr int B_KEMPTY = B_KFULL + kStages;
 constexpr int B_SFULL = B_KEMPTY + kStages;
-constexpr int B_SEMPTY = B_SFULL + 2;
-constexpr int B_PFULL = B_SEMPTY + 2;
-constexpr int B_PEMPTY = B_PFULL + 2;
-constexpr int B_XFULL = B_PEMPTY + 2;
-constexpr int B_XEMPTY = B_XFULL + 2;
-constexpr int B_PVDONE = B_XEMPTY + 2;
+constexpr int B_PFULL = B_SFULL + 2;
+constexpr int B_XFULL = B_PFULL + 2;
+constexpr int B_PVDONE = B_XFULL + 2;
 constexpr int B_OFINAL = B_PVDONE + 1;
 constexpr int B_QREADY = B_OFINAL + 1;
 constexpr int B_DRAIN = B_QREADY + 1;
@@ -118,24 +117,42 @@ __device__ __forceinline__ void drain_bar(const Ctx &c, uint32_t bar, uint32_t p
 // ----------------------------------------------------------------------------
 // TMA producer: gathers this CTA's half of every page of the part.
 // ----------------------------------------------------------------------------
+__device__ __forceinline__ int checked_phys(const DecodeParams &p, int b, int blk) {
+    int phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + blk);
+    if (phys < 0 || phys >= p.num_blocks) {
+        atomicOr(p.err, kErrBadBlock);
+        phys = 0;
+    }
+    return phys;
+}
+
 __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtensorMap *km128,
                               const CUtensorMap *km64, const int32_t *rec, int cta, int hk,
                               uint64_t policy) {
+    // L2 prefetch runs kPrefetchPages ahead of the shared-memory loads, so a
+    // load finds its tile in L2 and the short ring only covers L2 latency.
+    PageCursor ahead;
+    ahead.init(rec, p);
+    auto prefetch = [&](const PageCursor &pc) {
+        const int phys = checked_phys(p, pc.s.b, pc.blk);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) tma_prefetch_l2_4d(km128, 256 * cta + 64 * a, hk, 0, phys);
+        tma_prefetch_l2_4d(km64, 512 + 32 * cta, hk, 0, phys);
+    };
+    for (int k = 0; k < kPrefetchPages && ahead.valid; ++k) {
+        prefetch(ahead);
+        ahead.advance(p);
+    }
     SegmentWalk walk;
     walk.init(rec);
     Segment s;
     uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
-        const int32_t *bt_row = p.block_table + (int64_t)s.b * p.bt_stride;
         for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
             const uint32_t st = it % kStages;
             if (!wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u)) { ok = false; break; }
-            int phys = __ldg(bt_row + blk);
-            if (phys < 0 || phys >= p.num_blocks) {
-                atomicOr(p.err, kErrBadBlock);
-                phys = 0;
-            }
+            const int phys = checked_phys(p, s.b, blk);
             const uint32_t full = bar_addr(c, B_KFULL + st);
             const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
             mbar_arrive_expect_tx(full, kHalfBytes);
@@ -144,6 +161,10 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
             for (int a = 0; a < 4; ++a)
                 tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
             tma_load_4d(dst + 32768u, km64, full, 512 + 32 * cta, hk, 0, phys, policy);
+            if (ahead.valid) {
+                prefetch(ahead);
+                ahead.advance(p);
+            }
         }
     }
     // Drain: every copy issued must have landed before the CTA may exit.
@@ -162,16 +183,14 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
     tc_fence_after();
     if (lane == 0) {
         constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
-        const uint32_t pbase = c.base + OFF_P + pb * 16384u;
         const uint32_t vbase = c.base + OFF_K + st * kHalfBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = make_sdesc(pbase + kk * 32u, 16, 1024, kSwizzle128B);
+            // P (bf16 pairs, 16 keys = 8 columns per k-step) lives where its S was
             const uint64_t bd = make_sdesc(vbase + kk * 2048u, 8192, 1024, kSwizzle128B);
-            umma_ss(tmem + TM_O, ad, bd, idPV, (first_of_seg && kk == 0) ? 0u : 1u);
+            umma_ts(tmem + TM_O, tmem + TM_S + 64u * pb + 8u * kk, bd, idPV, (first_of_seg && kk == 0) ? 0u : 1u);
         }
         umma_commit(bar_addr(c, B_KEMPTY + st));
-        umma_commit(bar_addr(c, B_PEMPTY + pb));
         umma_commit(bar_addr(c, B_PVDONE));
     }
     __syncwarp();
@@ -211,8 +230,8 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SEMPTY + sb), ((it >> 1) & 1u) ^ 1u));
-            if (!ok) break;
+            // Buffer sb last held S/P of page it-2; PV(it-2) was issued before
+            // this S (tcgen05 MMAs of one thread execute in issue order).
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t dS = tmem + TM_S + 64u * sb;
@@ -263,12 +282,11 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 
     // shared addresses
     const uint32_t xrow_local[2] = {c.base + OFF_X + r * 256u, c.base + OFF_X + 32768u + r * 256u};
-    uint32_t xrow_peer[2], xfull_peer[2], xempty_peer[2];
+    uint32_t xrow_peer[2], xfull_peer[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         xrow_peer[k] = mapa_shared(xrow_local[k], peer);
         xfull_peer[k] = mapa_shared(bar_addr(c, B_XFULL + k), peer);
-        xempty_peer[k] = mapa_shared(bar_addr(c, B_XEMPTY + k), peer);
     }
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 
@@ -311,40 +329,48 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), ph));
             if (!ok) break;
             tc_fence_after();
+            if (!warp_active) {
+                // rows with no query: P = 0 so that their O rows stay finite
+                uint32_t z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0u;
+                tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, z);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar_addr(c, B_PFULL + sb));
+                continue;
+            }
             float sv[64];
-            if (warp_active) {
+            {
                 uint32_t raw[64];
                 tmem_ld_32x32b_x64(tmem + lane_base + TM_S + 64u * sb, raw);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(c, B_SEMPTY + sb));
-            if (!warp_active) {
-                mbar_arrive(bar_addr(c, B_PFULL + sb));
-                continue;
-            }
-            // ---- exchange partial logits with the peer CTA
-            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XEMPTY + sb), ph ^ 1u));
-            if (!ok) break;
+            // ---- exchange partial logits with the peer CTA.  Arm our buffer for
+            // the peer's 256 bytes of this row, send ours with st.async (byte
+            // count lands on the peer's barrier), then wait for the peer's.
+            // The peer can only send page it+2 into this buffer after it has
+            // received our page it+1, which we send after reading this one,
+            // so no "buffer free" handshake is needed.
+            mbar_arrive_expect_tx(bar_addr(c, B_XFULL + sb), 256u);
+            {
+                const uint32_t dst = sb ? xrow_peer[1] : xrow_peer[0];
+                const uint32_t pbar = sb ? xfull_peer[1] : xfull_peer[0];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const uint32_t a = xrow_peer[sb] + ((uint32_t)(ch ^ (r & 7)) << 4);
-                asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-                             :: "r"(a), "f"(sv[4 * ch]), "f"(sv[4 * ch + 1]), "f"(sv[4 * ch + 2]), "f"(sv[4 * ch + 3])
-                             : "memory");
+                for (int ch = 0; ch < 16; ++ch)
+                    st_async_v4(dst + ((uint32_t)(ch ^ (r & 7)) << 4), sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2],
+                                sv[4 * ch + 3], pbar);
             }
-            mbar_arrive_remote(xfull_peer[sb]);
             ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XFULL + sb), ph));
             if (!ok) break;
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
-                    smem_gen + (xrow_local[sb] - c.base) + ((ch ^ (r & 7)) << 4));
+                    smem_gen + ((sb ? xrow_local[1] : xrow_local[0]) - c.base) + ((ch ^ (r & 7)) << 4));
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
-            mbar_arrive_remote(xempty_peer[sb]);
 
             // ---- mask + scale (log2 domain) + page max
             const int nv = n_vis - blk * kPage;   // visible keys of this row in this page
@@ -372,14 +398,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
             }
             l_sum += psum;
-            // ---- P row -> smem (K-major SW128), once PV(it - 2) released the buffer
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PEMPTY + sb), ph ^ 1u));
-            if (!ok) break;
-            uint8_t *prow = smem_gen + OFF_P + sb * 16384u;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(prow + swz128_offset(r, ch)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns)
+            tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, pk);
             // ---- lazy O correction, after PV(it - 1) has landed in TMEM
             if (__any_sync(0xffffffffu, raise && o_live)) {
                 ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PVDONE), (it - 1) & 1u));
@@ -394,9 +414,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                     for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
                     tmem_st_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
                 }
-                tmem_st_wait();
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_addr(c, B_PFULL + sb));
         }
@@ -486,11 +505,8 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, B_SFULL + i), 1);
-            mbar_init(bar_addr(c, B_SEMPTY + i), 128);
             mbar_init(bar_addr(c, B_PFULL + i), 128);
-            mbar_init(bar_addr(c, B_PEMPTY + i), 1);
-            mbar_init(bar_addr(c, B_XFULL + i), 32 * nwa);
-            mbar_init(bar_addr(c, B_XEMPTY + i), 32 * nwa);
+            mbar_init(bar_addr(c, B_XFULL + i), 32 * nwa);   // + 256 B of st.async per arrival
         }
         mbar_init(bar_addr(c, B_PVDONE), 1);
         mbar_init(bar_addr(c, B_OFINAL), 1);
@@ -506,10 +522,6 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
-    // P buffers start at zero: rows of warps without real rows are never written.
-    for (uint32_t i = threadIdx.x; i < 2 * 16384 / 16; i += blockDim.x)
-        *reinterpret_cast<uint4 *>(smem + OFF_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
