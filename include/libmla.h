@@ -195,6 +195,36 @@ int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_ca
                        void *workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * Size of the scratch built into the library for mla_decode_fwd_noalloc:
+ * 64 MiB of device memory on every GPU that loads the library, held until
+ * the process exits.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * mla_decode_fwd without a workspace argument, for callers that cannot
+ * allocate device memory themselves: code whose device memory is owned by
+ * another allocator (an inference server's pool, say) or a latency-critical
+ * loop that cannot afford the device-wide synchronisation cudaMalloc or
+ * cudaFree may cause.  The split partials go to a scratch array built into
+ * the library (MLA_NOALLOC_SCRATCH_BYTES); this call allocates nothing.
+ * The pages this library follows have no counterpart of this call.
+ *
+ * Arguments, results and errors as mla_decode_fwd, plus MLA_ERR_UNSUPPORTED
+ * (with a message giving both sizes) when mla_workspace_size(shape) exceeds
+ * MLA_NOALLOC_SCRATCH_BYTES.  The first call on a device looks up the
+ * scratch's device address with that device current; make it before any
+ * stream capture.  All calls share the one scratch array: calls whose
+ * kernels may overlap on the GPU (unordered streams) race on it and must not
+ * be issued.  Nothing in the scratch needs clearing between calls.
+ */
+int mla_decode_fwd_noalloc(const mla_shape_t *shape, const void *q, const void *k_cache,
+                           const int32_t *block_table, const int32_t *cache_seqlens,
+                           const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                           float softmax_scale, int causal, void *out, float *softmax_lse,
+                           mla_stream_t stream);
+
+/*
  * Synchronizes the current device, then stores in *bits the OR of the
  * MLA_DEVERR_* bits kernels of this library raised on it since the last
  * clear, and clears them when `clear` is non-zero.  Returns MLA_OK, or

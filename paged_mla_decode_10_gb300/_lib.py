@@ -25,6 +25,7 @@ MLA_ERR_DEVICE = 6
 MLA_DEVERR_TIMEOUT = 1
 MLA_DEVERR_BAD_BLOCK = 2
 MLA_METADATA_SIZE = 8
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class MlaShape(ctypes.Structure):
@@ -73,6 +74,8 @@ def load():
     for name in ("mla_decode_fwd", "mla_decode_splitkv", "mla_decode_combine"):
         getattr(L, name).argtypes = dec
         getattr(L, name).restype = c_int
+    L.mla_decode_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
+    L.mla_decode_fwd_noalloc.restype = c_int
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]
     for name in ("mla_get_num_sm_parts", "mla_get_metadata", "mla_workspace_size", "mla_check_device_error"):
         getattr(L, name).restype = c_int

@@ -297,6 +297,12 @@ int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t strea
 
 }  // namespace
 
+namespace mla {
+// Records `msg` as the calling thread's last error (mla_last_error) and
+// returns `status`; for entry points defined in other files.
+int report_error(int status, const char *msg) { return fail(status, "%s", msg); }
+}  // namespace mla
+
 extern "C" {
 
 int mla_version(void) { return 100; }
