@@ -19,6 +19,7 @@ __global__ void mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, co
 __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
 __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
 uint32_t splitkv_smem_bytes();
+uint32_t splitkv_threads();
 }  // namespace mla
 
 // Error bits raised by the kernels on this device (MLA_DEVERR_*).
@@ -87,7 +88,7 @@ int device_state(DeviceState **out) {
                 return cuda_fail(e, "cudaFuncSetAttribute(metadata)");
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 64, 1, 1);
-            cfg.blockDim = dim3(192, 1, 1);
+            cfg.blockDim = dim3(splitkv_threads(), 1, 1);
             cfg.dynamicSmemBytes = smem;
             int clusters = 0;
             e = cudaOccupancyMaxActiveClusters(&clusters, (void *)mla_splitkv_kernel, &cfg);
@@ -281,7 +282,7 @@ int launch_splitkv(const mla_shape_t *sh, const void *k_cache, const Prepared &p
     CUtensorMap m128, m64;
     int st = kcache_maps(sh, k_cache, &m128, &m64);
     if (st != MLA_OK) return st;
-    mla_splitkv_kernel<<<pr.grid, 192, splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
+    mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
     return MLA_OK;

@@ -25,8 +25,9 @@
 //   P (bf16) is written back over the S buffer it came from and read by the
 //   PV MMA straight from TMEM.
 //   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
-//   warp  4    TMA producer (one lane): page gather through block_table
-//   warp  5    MMA issuer (one lane) + TMEM allocation
+//   warps 4-7  logit exchange: S out of TMEM, staged, DMA'd to the peer
+//   warp  8    TMA producer (one lane): page gather through block_table
+//   warp  9    MMA issuer (one lane) + TMEM allocation
 //
 // Online softmax (log2 domain) with lazy rescaling: the running max is only
 // raised when a page's max exceeds it by more than 8 (a factor of 256), so
@@ -46,24 +47,30 @@ namespace mla {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kPrefetchPages = 8;               // L2 prefetch distance of the producer
 constexpr uint32_t kHalfBytes = 36864;          // one CTA's 288-dim half of a page
+constexpr uint32_t kXBytes = 32768;             // one 128 x 64 fp32 partial-logit tile
 constexpr uint32_t OFF_QR = 0;                  // 128 rows x 64 B, SW64
 constexpr uint32_t OFF_K = 8192;
-constexpr uint32_t OFF_X = OFF_K + kStages * kHalfBytes;
-constexpr uint32_t OFF_BAR = OFF_X + 2 * 32768;
+constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (2 slots)
+constexpr uint32_t OFF_XOUT = OFF_XIN + 2 * kXBytes;          // our partial tile, staged for the DMA
+constexpr uint32_t OFF_BAR = OFF_XOUT + kXBytes;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kThreads = 320;                   // 10 warps, roles below
 
 // barrier indices
 constexpr int B_KFULL = 0;
 constexpr int B_KEMPTY = B_KFULL + kStages;
 constexpr int B_SFULL = B_KEMPTY + kStages;
-constexpr int B_PFULL = B_SFULL + 2;
-constexpr int B_XFULL = B_PFULL + 2;
-constexpr int B_PVDONE = B_XFULL + 2;
+constexpr int B_SREAD = B_SFULL + 2;            // exchange warps have read S out of TMEM
+constexpr int B_PFULL = B_SREAD + 2;
+constexpr int B_XFULL = B_PFULL + 2;            // peer's partial tile has landed in XIN
+constexpr int B_XINFREE = B_XFULL + 2;          // peer has read the tile we sent into its XIN slot
+constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received our last tile: XOUT reusable
+constexpr int B_PVDONE = B_STAGEFREE + 1;
 constexpr int B_OFINAL = B_PVDONE + 1;
 constexpr int B_QREADY = B_OFINAL + 1;
 constexpr int B_DRAIN = B_QREADY + 1;
@@ -183,13 +190,13 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
     tc_fence_after();
     if (lane == 0) {
         constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
-        const uint32_t vbase = c.base + OFF_K + st * kHalfBytes;
+        // V of this stage, MN-major: 4 boxes of 64 dims (LBO 8 KB), 8-key groups 1 KB apart
+        const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
+        const uint32_t pa = tmem + TM_S + 64u * pb;   // P (bf16 pairs, 8 columns per 16 keys) where its S was
+        umma_ts(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            // P (bf16 pairs, 16 keys = 8 columns per k-step) lives where its S was
-            const uint64_t bd = make_sdesc(vbase + kk * 2048u, 8192, 1024, kSwizzle128B);
-            umma_ts(tmem + TM_O, tmem + TM_S + 64u * pb + 8u * kk, bd, idPV, (first_of_seg && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 1; kk < 4; ++kk)   // +16 keys = +2048 B = +128 in the descriptor's 16-byte units
+            umma_ts(tmem + TM_O, pa + 8u * kk, bd0 + 128u * kk, idPV, 1u);
         umma_commit(bar_addr(c, B_KEMPTY + st));
         umma_commit(bar_addr(c, B_PVDONE));
     }
@@ -235,17 +242,16 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t dS = tmem + TM_S + 64u * sb;
+                // K-major page boxes: +32 B per 16-dim k-step, +8 KB per 64-dim box (16-byte units)
+                const uint64_t bk = make_sdesc(stage, 16, 1024, kSwizzle128B);
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bd = make_sdesc(stage + (kk >> 2) * 8192u + (kk & 3) * 32u, 16, 1024, kSwizzle128B);
-                    umma_ts(dS, tmem + TM_Q + 8u * kk, bd, idS, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t ad = make_sdesc(c.base + OFF_QR + kk * 32u, 16, 512, kSwizzle64B);
-                    const uint64_t bd = make_sdesc(stage + 32768u + kk * 32u, 16, 512, kSwizzle64B);
-                    umma_ss(dS, ad, bd, idS, 1u);
-                }
+                for (int kk = 0; kk < 16; ++kk)
+                    umma_ts(dS, tmem + TM_Q + 8u * kk, bk + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idS,
+                            kk > 0 ? 1u : 0u);
+                const uint64_t aq = make_sdesc(c.base + OFF_QR, 16, 512, kSwizzle64B);
+                const uint64_t br = make_sdesc(stage + 32768u, 16, 512, kSwizzle64B);
+                umma_ss(dS, aq, br, idS, 1u);
+                umma_ss(dS, aq + 2u, br + 2u, idS, 1u);
                 umma_commit(bar_addr(c, B_SFULL + sb));
             }
             __syncwarp();
@@ -266,6 +272,68 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
 }
 
 // ----------------------------------------------------------------------------
+// Exchange warps (4-7): ship this CTA's partial logit tile to the peer CTA.
+// Warp 4+q owns TMEM lane quadrant q, thread (4+q, l) row r = 32q + l: it
+// copies its row of S out of TMEM into the staging tile XOUT, and lane 0
+// hands the warp's 32 rows (8 KB) to the DMA engine, which writes them into
+// the peer's XIN slot and counts the bytes on the peer's XFULL.  The DMA, not
+// the SM's load/store pipe, carries the traffic.  XOUT is rewritten once the
+// peer has received the previous tile (STAGEFREE); an XIN slot once the peer
+// has read what it held (XINFREE).
+// ----------------------------------------------------------------------------
+__device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem, int cta,
+                              int rb) {
+    const int q = (int)(threadIdx.x >> 5) - 4;
+    const int lane = threadIdx.x & 31;
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
+    const uint32_t peer = (uint32_t)(cta ^ 1);
+    const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
+    const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
+    uint8_t *row = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT + (uint32_t)r * 256u;
+
+    SegmentWalk walk;
+    walk.init(rec);
+    Segment s;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
+            const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + b), ph));
+            if (!ok) break;
+            if (!active) {
+                if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
+                continue;
+            }
+            tc_fence_after();
+            uint32_t raw[64];
+            tmem_ld_32x32b_x64(tmem + lane_base + TM_S + 64u * b, raw);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
+            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
+            if (!ok) break;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch)
+                *reinterpret_cast<uint4 *>(row + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+            if (!ok) break;
+            if (lane == 0)
+                bulk_copy_to_peer(xin_peer + b * kXBytes, c.base + OFF_XOUT + (uint32_t)q * 8192u, 8192u,
+                                  b ? xfull_peer[1] : xfull_peer[0]);
+        }
+    }
+    // Drain: the last tile sent must have landed before the CTAs may exit.
+    if (active && it > 0u) drain_bar(c, bar_addr(c, B_STAGEFREE), (it - 1u) & 1u);
+}
+
+// ----------------------------------------------------------------------------
 // Softmax / epilogue warps (thread r owns query row r of the 128-row block).
 // ----------------------------------------------------------------------------
 __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem,
@@ -281,13 +349,10 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const uint32_t peer = (uint32_t)(cta ^ 1);
 
     // shared addresses
-    const uint32_t xrow_local[2] = {c.base + OFF_X + r * 256u, c.base + OFF_X + 32768u + r * 256u};
-    uint32_t xrow_peer[2], xfull_peer[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        xrow_peer[k] = mapa_shared(xrow_local[k], peer);
-        xfull_peer[k] = mapa_shared(bar_addr(c, B_XFULL + k), peer);
-    }
+    const uint32_t xrow_local[2] = {c.base + OFF_XIN + r * 256u, c.base + OFF_XIN + kXBytes + r * 256u};
+    const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE), peer),
+                                    mapa_shared(bar_addr(c, B_XINFREE + 1), peer)};
+    const uint32_t stagefree_peer = mapa_shared(bar_addr(c, B_STAGEFREE), peer);
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 
     SegmentWalk walk;
@@ -348,29 +413,20 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
             }
-            // ---- exchange partial logits with the peer CTA.  Arm our buffer for
-            // the peer's 256 bytes of this row, send ours with st.async (byte
-            // count lands on the peer's barrier), then wait for the peer's.
-            // The peer can only send page it+2 into this buffer after it has
-            // received our page it+1, which we send after reading this one,
-            // so no "buffer free" handshake is needed.
-            mbar_arrive_expect_tx(bar_addr(c, B_XFULL + sb), 256u);
-            {
-                const uint32_t dst = sb ? xrow_peer[1] : xrow_peer[0];
-                const uint32_t pbar = sb ? xfull_peer[1] : xfull_peer[0];
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch)
-                    st_async_v4(dst + ((uint32_t)(ch ^ (r & 7)) << 4), sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2],
-                                sv[4 * ch + 3], pbar);
-            }
+            // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
+            // add, then tell the peer its staging buffer (and our XIN slot) is free
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + sb), 8192u);
             ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XFULL + sb), ph));
             if (!ok) break;
+            if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
                     smem_gen + ((sb ? xrow_local[1] : xrow_local[0]) - c.base) + ((ch ^ (r & 7)) << 4));
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
+            __syncwarp();
+            if ((r & 31) == 0) mbar_arrive_remote_relaxed(sb ? xfree_peer[1] : xfree_peer[0]);
 
             // ---- mask + scale (log2 domain) + page max
             const int nv = n_vis - blk * kPage;   // visible keys of this row in this page
@@ -398,7 +454,11 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
             }
             l_sum += psum;
-            // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns)
+            // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
+            // once the exchange warps have copied that S out
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), ph));
+            if (!ok) break;
+            tc_fence_after();
             tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, pk);
             // ---- lazy O correction, after PV(it - 1) has landed in TMEM
             if (__any_sync(0xffffffffu, raise && o_live)) {
@@ -476,7 +536,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 
 }  // namespace
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
                    const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -505,20 +565,23 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, B_SFULL + i), 1);
+            mbar_init(bar_addr(c, B_SREAD + i), 4);
             mbar_init(bar_addr(c, B_PFULL + i), 128);
-            mbar_init(bar_addr(c, B_XFULL + i), 32 * nwa);   // + 256 B of st.async per arrival
+            mbar_init(bar_addr(c, B_XFULL + i), nwa);       // + 8 KB of DMA per arrival
+            mbar_init(bar_addr(c, B_XINFREE + i), nwa);     // remote arrivals from the peer
         }
+        mbar_init(bar_addr(c, B_STAGEFREE), nwa);           // remote arrivals from the peer
         mbar_init(bar_addr(c, B_PVDONE), 1);
         mbar_init(bar_addr(c, B_OFINAL), 1);
         mbar_init(bar_addr(c, B_QREADY), 128);
         mbar_init(bar_addr(c, B_DRAIN), 1);
         fence_mbar_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&km128);
         tma_prefetch_desc(&km64);
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -531,7 +594,9 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
 
     if (warp < 4) {
         softmax_role(c, p, rec, tmem, cta, rb, hk);
-    } else if (warp == 4) {
+    } else if (warp < 8) {
+        exchange_role(c, p, rec, tmem, cta, rb);
+    } else if (warp == 8) {
         if (lane == 0) {
             const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
             producer_role(c, p, &km128, &km64, rec, cta, hk, pol);
@@ -543,11 +608,12 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == 9) tmem_dealloc(tmem, 512);
     cluster_arrive();   // no CTA leaves while its peer may still touch its shared memory
     cluster_wait();
 }
 
 uint32_t splitkv_smem_bytes() { return kSmemBytes; }
+uint32_t splitkv_threads() { return kThreads; }
 
 }  // namespace mla
