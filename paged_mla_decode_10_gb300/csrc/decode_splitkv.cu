@@ -95,19 +95,13 @@ __device__ __noinline__ void raise_timeout(const Ctx &c) {
 }
 
 // Bounded wait; false when it timed out or another role already aborted.
+// CTA-scope acquire suffices for every barrier here: XFULL completes by the
+// peer's bulk copy landing in this CTA's shared memory (like a TMA load), and
+// the barriers the peer arrives on remotely (XINFREE, STAGEFREE) carry no data.
 __device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
-        if (*c.abort_flag) return false;
-        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
-    }
-    return true;
-}
-__device__ __forceinline__ bool wait_bar_cluster(const Ctx &c, uint32_t bar, uint32_t parity) {
-    if (mbar_test_cluster(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_test_cluster(bar, parity)) {
         if (*c.abort_flag) return false;
         if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
     }
@@ -314,7 +308,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
-            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
             if (!ok) break;
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch)
@@ -322,7 +316,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
                     make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
             fence_proxy_async_smem();
             __syncwarp();
-            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
             if (!ok) break;
             if (lane == 0)
                 bulk_copy_to_peer(xin_peer + b * kXBytes, c.base + OFF_XOUT + (uint32_t)q * 8192u, 8192u,
@@ -416,7 +410,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
             // add, then tell the peer its staging buffer (and our XIN slot) is free
             if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + sb), 8192u);
-            ok = __all_sync(0xffffffffu, wait_bar_cluster(c, bar_addr(c, B_XFULL + sb), ph));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + sb), ph));
             if (!ok) break;
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
 #pragma unroll
@@ -428,14 +422,17 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             __syncwarp();
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(sb ? xfree_peer[1] : xfree_peer[0]);
 
-            // ---- mask + scale (log2 domain) + page max
+            // ---- mask (only pages the row does not see whole) + page max, on the raw
+            // logits; the scale (> 0) is applied inside the exponent below
             const int nv = n_vis - blk * kPage;   // visible keys of this row in this page
-            float mt = -INFINITY;
+            if (__any_sync(0xffffffffu, nv < 64)) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                sv[j] = j < nv ? sv[j] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[j]);
+                for (int j = 0; j < 64; ++j) sv[j] = j < nv ? sv[j] : -INFINITY;
             }
+            float mraw = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mraw = fmaxf(mraw, sv[j]);
+            const float mt = mraw * p.scale_log2;   // -inf stays -inf
             const bool o_live = m_ref != -INFINITY;
             const bool raise = mt > m_ref + kRescaleThreshold;  // true for the first finite page
             float factor = 1.f;
@@ -444,12 +441,14 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 m_ref = mt;
                 l_sum *= factor;
             }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            const float c2 = p.scale_log2;
             uint32_t pk[32];
             float psum = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = ex2_approx(sv[2 * j] - m_use), p1 = ex2_approx(sv[2 * j + 1] - m_use);
+                const float p0 = ex2_approx(fmaf(sv[2 * j], c2, neg_m));
+                const float p1 = ex2_approx(fmaf(sv[2 * j + 1], c2, neg_m));
                 pk[j] = pack_bf16x2(p0, p1);
                 psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
             }
