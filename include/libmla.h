@@ -83,8 +83,8 @@ enum {
  * h_q % h_k == 0, head_dim == 576, head_dim_v == 512, page_block_size == 64,
  * num_blocks >= 1, max_blocks_per_seq >= 1, num_sm_parts >= 1; every stride a
  * multiple of 8 elements and every bf16 base pointer 16-byte aligned.
- * Limit (else MLA_ERR_UNSUPPORTED): s_q * h_q / h_k <= 1024 query rows per
- * KV head.
+ * Limits (else MLA_ERR_UNSUPPORTED): s_q * h_q / h_k <= 1024 query rows per
+ * KV head; batch <= 65535.
  */
 typedef struct {
     int32_t batch;

@@ -20,6 +20,7 @@ __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
 __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
 uint32_t splitkv_smem_bytes();
 uint32_t splitkv_threads();
+uint32_t combine_threads();
 }  // namespace mla
 
 // Error bits raised by the kernels on this device (MLA_DEVERR_*).
@@ -205,6 +206,7 @@ int check_shape(const mla_shape_t *sh) {
         return fail(MLA_ERR_ARG, "num_blocks and max_blocks_per_seq must be >= 1");
     if (sh->num_sm_parts < 1) return fail(MLA_ERR_ARG, "num_sm_parts must be >= 1");
     const long long rows = (long long)sh->s_q * sh->h_q / sh->h_k;
+    if (sh->batch > 65535) return fail(MLA_ERR_UNSUPPORTED, "batch %d exceeds 65535", sh->batch);
     if (rows > kMaxRowsPerHead)
         return fail(MLA_ERR_UNSUPPORTED, "s_q*h_q/h_k = %lld query rows per KV head exceeds %d", rows, kMaxRowsPerHead);
     for (int i = 0; i < 3; ++i) {
@@ -289,8 +291,8 @@ int launch_splitkv(const mla_shape_t *sh, const void *k_cache, const Prepared &p
 }
 
 int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t stream) {
-    const dim3 grid(sh->batch, sh->h_k, (pr.p.rows + 7) / 8);
-    mla_combine_kernel<<<grid, 256, 0, stream>>>(pr.p);
+    const dim3 grid(pr.p.rows, sh->batch, sh->h_k);
+    mla_combine_kernel<<<grid, combine_threads(), 0, stream>>>(pr.p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return MLA_OK;
