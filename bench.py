@@ -328,6 +328,14 @@ def run_libmla(args, w, world, rank, local):
     c_ms = [b.elapsed_time(c) for _, b, c in ev3]
     kernel_ms = reduce_max(sum(k_ms) / len(k_ms), world, dev)
     combine_ms = sum(c_ms) / len(c_ms)
+    # ---- the schedule (mla_get_metadata) on its own: amortised over the layers of a step
+    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        evm[i][0].record(stream)
+        M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=parts)
+        evm[i][1].record(stream)
+    torch.cuda.synchronize()
+    metadata_us = 1e3 * sum(a.elapsed_time(b) for a, b in evm) / args.steps
     bits = M.mla_check_device_error(clear=True)
     if bits:
         raise RuntimeError(f"device error bits {bits} during the benchmark")
@@ -405,6 +413,7 @@ def run_libmla(args, w, world, rank, local):
                      "unit": unit, "frac": achieved / peak, "traffic": traffic, "peak_source": peaks_src,
                      "kernel_us": kernel_ms * 1e3, "combine_us": combine_ms * 1e3,
                      "algorithmic_per_launch": nbytes if bound == "hbm" else flop},
+        "metadata_us": metadata_us,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,

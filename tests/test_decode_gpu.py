@@ -71,6 +71,26 @@ def test_metadata_matches_policy_bit_exact():
         OM.check_metadata([int(x) for x in Ls], md.cpu().numpy(), ns.cpu().numpy())
 
 
+def test_metadata_bit_exact_on_random_small_cases():
+    """Zero-length sequences, sequences that end exactly on a part's target,
+    parts that outnumber blocks: the device walk must reproduce the policy."""
+    import paged_mla_decode_10_gb300 as M
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        B = int(rng.integers(1, 90))
+        L = rng.integers(0, 400, size=B)
+        L[rng.random(B) < 0.3] = 0
+        if trial % 3 == 0:
+            L = (rng.integers(0, 6, size=B) * 64).astype(np.int64)   # whole blocks: exact-target hits
+        parts = int(rng.integers(1, 100))
+        Ls = [int(x) for x in L]
+        Lt = torch.tensor(Ls, dtype=torch.int32, device="cuda")
+        md, ns = M.mla_get_metadata(Lt, 128, 1, num_sm_parts=parts)
+        md_ref, ns_ref = OM.schedule(Ls, parts)
+        np.testing.assert_array_equal(md.cpu().numpy(), md_ref, err_msg=f"trial {trial} L={Ls} parts={parts}")
+        np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
+
+
 def test_num_sm_parts_variation_consistent():
     inp = _custom("parts", 4, 1, 128, [3000, 100, 64, 2049], seed=9)
     ref_o, ref_l = oracle(inp)
