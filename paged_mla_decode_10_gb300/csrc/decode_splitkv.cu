@@ -20,13 +20,14 @@
 //
 // Per CTA:
 //   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
-//   smem  Q RoPE half (SW64) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
-//         36,864 B per page half) | S exchange double buffer (fp32) | mbarriers
+//   smem  Q RoPE half (SW64) | 3-stage page ring (4 x SW128 + 1 x SW64 boxes,
+//         36,864 B per page half) | S exchange: two landing slots and one
+//         staging tile (fp32) | epilogue staging | mbarriers
 //   P (bf16) is written back over the S buffer it came from and read by the
 //   PV MMA straight from TMEM.
 //   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
 //   warps 4-7  logit exchange: S out of TMEM, staged, DMA'd to the peer
-//   warp  8    TMA producer (one lane): page gather through block_table
+//   warp  8    TMA producer: page gather through block_table, Q prefetch
 //   warp  9    MMA issuer (one lane) + TMEM allocation
 //
 // Online softmax (log2 domain) with lazy rescaling: the running max is only
@@ -42,20 +43,22 @@
 
 #include "sm103.cuh"
 #include "decode_common.cuh"
+#include "decode_sync.cuh"
+#include "decode_epilogue.cuh"
 
 namespace mla {
 
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kPrefetchPages = 8;               // L2 prefetch distance of the producer
 constexpr uint32_t kHalfBytes = 36864;          // one CTA's 288-dim half of a page
 constexpr uint32_t kXBytes = 32768;             // one 128 x 64 fp32 partial-logit tile
 constexpr uint32_t OFF_QR = 0;                  // 128 rows x 64 B, SW64
 constexpr uint32_t OFF_K = 8192;
 constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (2 slots)
 constexpr uint32_t OFF_XOUT = OFF_XIN + 2 * kXBytes;          // our partial tile, staged for the DMA
-constexpr uint32_t OFF_BAR = OFF_XOUT + kXBytes;
+constexpr uint32_t OFF_EPI = OFF_XOUT + kXBytes;          // epilogue staging, one tile per softmax warp
+constexpr uint32_t OFF_BAR = OFF_EPI + 4 * kEpiWarpBytes;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -79,98 +82,61 @@ static_assert(B_COUNT <= 64, "barrier area");
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
-constexpr long long kTimeoutCycles = 4000000000ll;
 
-struct Ctx {
-    uint32_t base;              // shared address of the aligned smem base
-    volatile int *abort_flag;
-    int *err;
-};
-
-__device__ __forceinline__ uint32_t bar_addr(const Ctx &c, int i) { return c.base + OFF_BAR + 8u * i; }
-
-__device__ __noinline__ void raise_timeout(const Ctx &c) {
-    *c.abort_flag = 1;
-    atomicOr(c.err, kErrTimeout);
-}
-
-// Bounded wait; false when it timed out or another role already aborted.
-// CTA-scope acquire suffices for every barrier here: XFULL completes by the
-// peer's bulk copy landing in this CTA's shared memory (like a TMA load), and
-// the barriers the peer arrives on remotely (XINFREE, STAGEFREE) carry no data.
-__device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
-    if (mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_test(bar, parity)) {
-        if (*c.abort_flag) return false;
-        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
-    }
-    return true;
-}
-// Teardown wait: ignores the abort flag (drains what is in flight), still bounded.
-__device__ __forceinline__ void drain_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_test(bar, parity)) {
-        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return; }
-    }
-}
+// The CTA-scope acquire of wait_bar suffices for every barrier here: XFULL
+// completes by the peer's bulk copy landing in this CTA's shared memory (like
+// a TMA load), and the barriers the peer arrives on remotely (XINFREE,
+// STAGEFREE) carry no data.
 
 // ----------------------------------------------------------------------------
-// TMA producer: gathers this CTA's half of every page of the part.
+// TMA producer (whole warp 8): gathers this CTA's half of every page of the
+// part.  The warp reads the block-table entries of up to 32 pages with one
+// coalesced load and lane 0 issues the copies.  When the walk enters a new
+// segment, the warp asks L2 for that segment's query rows, so that the
+// softmax warps' Q loads at the segment switch hit L2.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ int checked_phys(const DecodeParams &p, int b, int blk) {
-    int phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + blk);
-    if (phys < 0 || phys >= p.num_blocks) {
-        atomicOr(p.err, kErrBadBlock);
-        phys = 0;
-    }
-    return phys;
-}
-
 __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtensorMap *km128,
-                              const CUtensorMap *km64, const int32_t *rec, int cta, int hk,
+                              const CUtensorMap *km64, const int32_t *rec, int cta, int rb, int hk,
                               uint64_t policy) {
-    // L2 prefetch runs kPrefetchPages ahead of the shared-memory loads, so a
-    // load finds its tile in L2 and the short ring only covers L2 latency.
-    PageCursor ahead;
-    ahead.init(rec, p);
-    auto prefetch = [&](const PageCursor &pc) {
-        const int phys = checked_phys(p, pc.s.b, pc.blk);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) tma_prefetch_l2_4d(km128, 256 * cta + 64 * a, hk, 0, phys);
-        tma_prefetch_l2_4d(km64, 512 + 32 * cta, hk, 0, phys);
-    };
-    for (int k = 0; k < kPrefetchPages && ahead.valid; ++k) {
-        prefetch(ahead);
-        ahead.advance(p);
-    }
+    const int lane = threadIdx.x & 31;
     SegmentWalk walk;
     walk.init(rec);
     Segment s;
     uint32_t it = 0;
-    bool ok = true;
+    bool ok = true, first = true;
     while (ok && walk.next(p, s)) {
-        for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
-            const uint32_t st = it % kStages;
-            if (!wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u)) { ok = false; break; }
-            const int phys = checked_phys(p, s.b, blk);
-            const uint32_t full = bar_addr(c, B_KFULL + st);
-            const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
-            mbar_arrive_expect_tx(full, kHalfBytes);
-            // tensor map dims: {576 dims, h_k heads, 64 rows, num_blocks}
+        if (!first) prefetch_q_rows(p, s.b, rb, hk, cta, lane);
+        first = false;
+        for (int base = s.lo; base < s.hi && ok; base += 32) {
+            const int n = s.hi - base < 32 ? s.hi - base : 32;
+            const int mine = lane < n ? checked_phys(p, s.b, base + lane) : 0;
+            for (int k = 0; k < n; ++k) {
+                const int phys = __shfl_sync(0xffffffffu, mine, k);
+                if (lane == 0) {
+                    const uint32_t st = it % kStages;
+                    ok = wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u);
+                    if (ok) {
+                        const uint32_t full = bar_addr(c, B_KFULL + st);
+                        const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
+                        mbar_arrive_expect_tx(full, kHalfBytes);
+                        // tensor map dims: {576 dims, h_k heads, 64 rows, num_blocks}
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
-                tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
-            tma_load_4d(dst + 32768u, km64, full, 512 + 32 * cta, hk, 0, phys, policy);
-            if (ahead.valid) {
-                prefetch(ahead);
-                ahead.advance(p);
+                        for (int a = 0; a < 4; ++a)
+                            tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
+                        tma_load_4d(dst + 32768u, km64, full, 512 + 32 * cta, hk, 0, phys, policy);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++it;
             }
         }
     }
     // Drain: every copy issued must have landed before the CTA may exit.
-    const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
-    for (uint32_t j = first; j < it; ++j) drain_bar(c, bar_addr(c, B_KFULL + j % kStages), (j / kStages) & 1u);
+    if (lane == 0) {
+        const uint32_t first_j = it > (uint32_t)kStages ? it - kStages : 0u;
+        for (uint32_t j = first_j; j < it; ++j) drain_bar(c, bar_addr(c, B_KFULL + j % kStages), (j / kStages) & 1u);
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -266,6 +232,43 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
 }
 
 // ----------------------------------------------------------------------------
+// Q of a segment, loaded by the exchange warps: this CTA's 256 latent dims ->
+// TMEM (bf16 pairs, the A operand of the QK^T MMAs), its 32 RoPE dims -> smem
+// (SW64).  Warp 4+q moves query rows 32q..32q+31 (TMEM lane quadrant q), lane
+// l row 32q + l.  Every load is issued before the first store, so a row
+// arrives in one round trip (an L2 hit after the producer's prefetch).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p, uint32_t tmem_q, int q, int lane,
+                                            int rb, int cta, int hk, const Segment &sg) {
+    const int r = q * 32 + lane;
+    const int row_g = rb * kRowsPerBlock + r;
+    const bool row_real = row_g < p.rows;
+    const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(
+        p.q + (int64_t)sg.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
+    uint32_t w0[64], w1[64];
+    uint4 rope[4];
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+        const uint4 x = row_real ? __ldg(qrow + cta * 32 + v) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 y = row_real ? __ldg(qrow + cta * 32 + 16 + v) : make_uint4(0u, 0u, 0u, 0u);
+        w0[4 * v] = x.x; w0[4 * v + 1] = x.y; w0[4 * v + 2] = x.z; w0[4 * v + 3] = x.w;
+        w1[4 * v] = y.x; w1[4 * v + 1] = y.y; w1[4 * v + 2] = y.z; w1[4 * v + 3] = y.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rope[k] = row_real ? __ldg(qrow + 64 + cta * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+    tmem_st_32x32b_x64(tmem_q, w0);
+    tmem_st_32x32b_x64(tmem_q + 64u, w1);
+    uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz64_offset(r, k)) = rope[k];
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar_addr(c, B_QREADY));
+}
+
+// ----------------------------------------------------------------------------
 // Exchange warps (4-7): ship this CTA's partial logit tile to the peer CTA.
 // Warp 4+q owns TMEM lane quadrant q, thread (4+q, l) row r = 32q + l: it
 // copies its row of S out of TMEM into the staging tile XOUT, and lane 0
@@ -276,7 +279,7 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
 // has read what it held (XINFREE).
 // ----------------------------------------------------------------------------
 __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem, int cta,
-                              int rb) {
+                              int rb, int hk) {
     const int q = (int)(threadIdx.x >> 5) - 4;
     const int lane = threadIdx.x & 31;
     const int r = q * 32 + lane;
@@ -287,12 +290,16 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
     uint8_t *row = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT + (uint32_t)r * 256u;
 
+    const uint32_t tmem_q = tmem + lane_base + TM_Q;
+
     SegmentWalk walk;
     walk.init(rec);
-    Segment s;
-    uint32_t it = 0;
+    Segment s, s_next;
+    uint32_t it = 0, g = 0;
     bool ok = true;
-    while (ok && walk.next(p, s)) {
+    bool have = walk.next(p, s);
+    if (have) load_q_half(c, p, tmem_q, q, lane, rb, cta, hk, s);
+    while (ok && have) {
         for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
             const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + b), ph));
@@ -322,6 +329,19 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
                 bulk_copy_to_peer(xin_peer + b * kXBytes, c.base + OFF_XOUT + (uint32_t)q * 8192u, 8192u,
                                   b ? xfull_peer[1] : xfull_peer[0]);
         }
+        if (!ok) break;
+        // Q of the next segment, once every MMA of this one has completed; the
+        // softmax warps store this segment's output meanwhile
+        const bool have_next = walk.next(p, s_next);
+        if (have_next) {
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_OFINAL), g & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            load_q_half(c, p, tmem_q, q, lane, rb, cta, hk, s_next);
+        }
+        s = s_next;
+        have = have_next;
+        ++g;
     }
     // Drain: the last tile sent must have landed before the CTAs may exit.
     if (active && it > 0u) drain_bar(c, bar_addr(c, B_STAGEFREE), (it - 1u) & 1u);
@@ -355,30 +375,6 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     uint32_t it = 0, g = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
-        // ---- Q half -> TMEM (latent dims, bf16 pairs) and smem (RoPE dims, SW64)
-        {
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(
-                p.q + (int64_t)s.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t w[64];
-#pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    uint4 x = row_real ? __ldg(qrow + cta * 32 + half * 16 + v) : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
-                }
-                tmem_st_32x32b_x64(tmem + lane_base + TM_Q + 64u * half, w);
-            }
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint4 x = row_real ? __ldg(qrow + 64 + cta * 4 + ch) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz64_offset(r, ch)) = x;
-            }
-            tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_addr(c, B_QREADY));
-        }
         int n_vis = p.causal ? s.L - p.s_q + 1 + qi : s.L;
         n_vis = n_vis < 0 ? 0 : (n_vis > s.L ? s.L : n_vis);
         float m_ref = -INFINITY, l_sum = 0.f;
@@ -480,7 +476,9 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
         }
         if (!ok) break;
 
-        // ---- epilogue: normalise this CTA's O half and store
+        // ---- epilogue: normalise this CTA's O half and store (meanwhile the
+        // exchange warps load the next segment's Q, and its first QK^T and
+        // logit exchange run)
         ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_OFINAL), g & 1u));
         if (!ok) break;
         tc_fence_after();
@@ -497,32 +495,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             const bool slot_ok = s.slot >= 0 && s.slot < p.max_slots;
             if (!direct && !slot_ok && row_real) atomicOr(p.err, kErrBadBlock);
             const int64_t prow_idx = ((int64_t)s.slot * p.h_k + hk) * p.rows + row_g;
-#pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t o[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
-                tmem_ld_wait();
-                if (!row_real) continue;
-                if (direct) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        p.out + (int64_t)s.b * p.o_s0 + (int64_t)qi * p.o_s1 + (int64_t)qh * p.o_s2 + 256 * cta + 64 * q4);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        dst[v] = w;
-                    }
-                } else if (slot_ok) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow_idx * kDv + 256 * cta + 64 * q4);
-#pragma unroll
-                    for (int v = 0; v < 16; ++v)
-                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-                }
-            }
+            store_o_half(p, tmem + lane_base + TM_O, smem_gen + OFF_EPI + warp * kEpiWarpBytes, r & 31,
+                         rb * kRowsPerBlock + warp * 32, s.b, hk, cta, direct, slot_ok, s.slot, inv);
             if (row_real && cta == 0) {
                 if (direct) p.lse[((int64_t)s.b * p.h_q + qh) * p.s_q + qi] = lse_nat;
                 else if (slot_ok) p.ws_lse[prow_idx] = lse_nat;
@@ -543,6 +517,7 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
     Ctx c;
     c.base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (c.base - raw);
+    c.bars = c.base + OFF_BAR;
     c.abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     c.err = p.err;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
@@ -594,12 +569,10 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
     if (warp < 4) {
         softmax_role(c, p, rec, tmem, cta, rb, hk);
     } else if (warp < 8) {
-        exchange_role(c, p, rec, tmem, cta, rb);
+        exchange_role(c, p, rec, tmem, cta, rb, hk);
     } else if (warp == 8) {
-        if (lane == 0) {
-            const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
-            producer_role(c, p, &km128, &km64, rec, cta, hk, pol);
-        }
+        const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+        producer_role(c, p, &km128, &km64, rec, cta, rb, hk, pol);
     } else {
         mma_role(c, p, rec, tmem, lane);
     }

@@ -135,6 +135,11 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int32
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
                  :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
+// Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
 // L2 eviction-priority policies for the cache hint operand.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
