@@ -21,6 +21,7 @@ __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts
 uint32_t splitkv_smem_bytes();
 uint32_t splitkv_threads();
 uint32_t combine_threads();
+uint32_t combine_rows_per_block();
 }  // namespace mla
 
 // Error bits raised by the kernels on this device (MLA_DEVERR_*).
@@ -290,10 +291,22 @@ int launch_splitkv(const mla_shape_t *sh, const void *k_cache, const Prepared &p
     return MLA_OK;
 }
 
+// The combine is a programmatic dependent launch: its blocks may be scheduled
+// while the split-KV kernel drains and wait (griddepcontrol.wait) for its
+// results, which hides most of the launch gap between the two kernels.
 int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t stream) {
-    const dim3 grid(pr.p.rows, sh->batch, sh->h_k);
-    mla_combine_kernel<<<grid, combine_threads(), 0, stream>>>(pr.p);
-    cudaError_t e = cudaGetLastError();
+    const uint32_t rpb = combine_rows_per_block();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((pr.p.rows + rpb - 1) / rpb, sh->batch, sh->h_k);
+    cfg.blockDim = dim3(combine_threads(), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, pr.p);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return MLA_OK;
 }

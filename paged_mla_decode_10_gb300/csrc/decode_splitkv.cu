@@ -581,6 +581,10 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
     __syncthreads();
     tc_fence_after();
     if (warp == 9) tmem_dealloc(tmem, 512);
+    // Only now may the combine kernel (a programmatic dependent) be scheduled:
+    // its blocks waiting beside running CTAs slowed this kernel down, while
+    // this late trigger still overlaps its launch with the teardown.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     cluster_arrive();   // no CTA leaves while its peer may still touch its shared memory
     cluster_wait();
 }
