@@ -82,7 +82,7 @@ def load_peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("decode_splitkv.cu", "sm103.cuh", "decode_common.cuh"):
+    for f in ("decode_splitkv.cu", "sm103.cuh", "decode_common.cuh", "decode_sync.cuh", "decode_epilogue.cuh", "tmem_ldst.inc"):
         with open(os.path.join(ROOT, "paged_mla_decode_10_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
