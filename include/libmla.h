@@ -124,8 +124,8 @@ int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, 
  * num_blocks, 0, 0]; the part processes, for b in [begin_b, end_b], blocks
  * [b == begin_b ? begin_blk : 0, b == end_b ? end_blk : ceil(L_b / 64)).
  * Policy: greedy contiguous walk over (sequence, block) with a fixed cost of
- * 4 blocks per segment and a per-part target of
- * ceil((W + (num_sm_parts - 1) * 4) / num_sm_parts), W = sum(n_b + 4).
+ * 6 blocks per segment and a per-part target of
+ * ceil((W + (num_sm_parts - 1) * 6) / num_sm_parts), W = sum(n_b + 6).
  * Errors: MLA_ERR_ARG (NULL pointer, batch < 0, num_sm_parts < 1,
  * num_heads_per_head_k < 1, num_heads_k < 1), MLA_ERR_UNSUPPORTED
  * (batch > 16384), MLA_ERR_CUDA.

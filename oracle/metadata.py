@@ -37,7 +37,10 @@ from typing import List, Sequence, Tuple
 import numpy as np
 
 PAGE = 64
-FIXED_COST = 4
+# The per-segment cost, in 64-row blocks: a part's fixed work for each
+# sequence it opens (loading that sequence's queries, storing its output)
+# measured on the decode kernel as about six pages' time.
+FIXED_COST = 6
 RECORD = 8
 
 

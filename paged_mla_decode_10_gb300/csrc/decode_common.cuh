@@ -9,7 +9,7 @@ constexpr int kPage = 64;          // cache rows per physical block
 constexpr int kDqk = 576;          // q / cache row dims (512 latent + 64 RoPE)
 constexpr int kDv = 512;           // V dims (prefix of each cache row)
 constexpr int kMdSize = 8;         // int32 per scheduler record
-constexpr int kFixedCost = 4;      // schedule: cost of opening a segment, in blocks
+constexpr int kFixedCost = 6;      // schedule: cost of opening a segment, in blocks
 constexpr int kRowsPerBlock = 128; // query rows per CTA (tcgen05 M)
 
 // Device-side error bits (mirror MLA_DEVERR_* of the public header).

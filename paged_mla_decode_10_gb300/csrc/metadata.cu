@@ -6,7 +6,7 @@
 // The record and policy are this library's:
 //
 //   record of part p: [begin_b, begin_blk, end_b, end_blk, first_slot, num_blocks, 0, 0]
-//   n_b = ceil(max(L_b, 0) / 64); c = 4 (cost of opening a segment, in blocks)
+//   n_b = ceil(max(L_b, 0) / 64); c = 6 (cost of opening a segment, in blocks)
 //   W = sum_{n_b > 0} (n_b + c);  T = max(1, ceil((W + (parts - 1) c) / parts))
 //   parts walk the (b, blk) sequence in order; a part stops opening segments
 //   when T - load - c <= 0, takes min(remaining, T - load - c) blocks when it
