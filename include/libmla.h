@@ -159,7 +159,14 @@ int mla_workspace_size(const mla_shape_t *shape, size_t *bytes);
  * entries past ceil(L / 64) are never read; needed entries outside
  * [0, num_blocks) are not dereferenced and raise MLA_DEVERR_BAD_BLOCK.
  * workspace: device scratch of at least mla_workspace_size bytes, 256-byte
- * aligned, not used concurrently by another call.
+ * aligned, not used concurrently by another call.  workspace == NULL with
+ * workspace_bytes == 0 selects the library's own stream-ordered workspace:
+ * one buffer per (device, stream), allocated and grown with cudaMallocAsync
+ * on `stream` (calls on one stream share it; calls on different streams get
+ * different buffers) and released by mla_shutdown (the workspace
+ * convention of the FlashMLA-PyTorch / vLLM pages leaves the scratch to the
+ * library; the Ascend ATB page's size query plus caller buffer is the
+ * explicit form).
  * Errors: MLA_ERR_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_ARCH, MLA_ERR_WORKSPACE,
  * MLA_ERR_CUDA.  Launches two kernels: mla_decode_splitkv then
  * mla_decode_combine, with the same arguments.
@@ -223,6 +230,14 @@ int mla_decode_fwd_noalloc(const mla_shape_t *shape, const void *q, const void *
                            const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
                            float softmax_scale, int causal, void *out, float *softmax_lse,
                            mla_stream_t stream);
+
+/*
+ * Releases the internal workspaces that calls without a workspace allocated
+ * (synchronizing each device that holds one first).  Later such calls
+ * allocate again.  Not to be called while another thread uses the library.
+ * Errors: MLA_ERR_CUDA.
+ */
+int mla_shutdown(void);
 
 /*
  * Synchronizes the current device, then stores in *bits the OR of the

@@ -77,6 +77,8 @@ def load():
     L.mla_decode_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
     L.mla_decode_fwd_noalloc.restype = c_int
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]
+    L.mla_shutdown.argtypes = []
+    L.mla_shutdown.restype = c_int
     for name in ("mla_get_num_sm_parts", "mla_get_metadata", "mla_workspace_size", "mla_check_device_error"):
         getattr(L, name).restype = c_int
     _lib = L

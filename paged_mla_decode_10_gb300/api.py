@@ -161,6 +161,12 @@ def mla_check_device_error(clear: bool = True) -> int:
     return bits.value
 
 
+def mla_shutdown() -> None:
+    """Release the library's internal workspaces (those of calls made with workspace=NULL)."""
+    L = _lib.load()
+    check(L.mla_shutdown(), "mla_shutdown")
+
+
 # ---- the interface page's two functions -------------------------------------------------
 
 def get_mla_metadata(cache_seqlens: torch.Tensor, num_heads_per_head_k: int,

@@ -228,14 +228,60 @@ size_t workspace_bytes_for(const mla_shape_t *sh, size_t *lse_off) {
     return off + ((slots * rows * sizeof(float) + 255) & ~(size_t)255);
 }
 
+// Workspace for calls that pass none: one buffer per (device, stream),
+// allocated with cudaMallocAsync on that stream and grown the same way (the
+// smaller one released with cudaFreeAsync on the stream, after the work
+// already queued there).  Calls on one stream run in order, so they can share
+// the buffer; calls on different streams get different buffers.
+struct WsEntry {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+constexpr int kWsEntries = 32;
+std::mutex g_ws_mu;
+WsEntry g_ws[kWsEntries];
+
+int internal_workspace(const mla_shape_t *sh, cudaStream_t stream, void **ws, size_t *ws_bytes) {
+    int st = check_shape(sh);
+    if (st != MLA_OK) return st;
+    const size_t need = workspace_bytes_for(sh, nullptr);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    WsEntry *slot = nullptr;
+    for (auto &w : g_ws) {
+        if (w.ptr && w.device == dev && w.stream == stream) { slot = &w; break; }
+        if (!w.ptr && !slot) slot = &w;
+    }
+    if (!slot) return fail(MLA_ERR_UNSUPPORTED, "more than %d (device, stream) pairs use the internal workspace", kWsEntries);
+    if (slot->bytes < need) {
+        if (slot->ptr && (e = cudaFreeAsync(slot->ptr, stream)) != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(workspace)");
+        slot->ptr = nullptr;
+        slot->bytes = 0;
+        void *ptr = nullptr;
+        if ((e = cudaMallocAsync(&ptr, need, stream)) != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+        slot->ptr = ptr;
+        slot->bytes = need;
+        slot->device = dev;
+        slot->stream = stream;
+    }
+    *ws = slot->ptr;
+    *ws_bytes = slot->bytes;
+    return MLA_OK;
+}
+
 struct Prepared {
     DecodeParams p;
     dim3 grid;
 };
 
-int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int32_t *block_table,
-            const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale, int causal,
-            void *out, float *lse, void *ws, size_t ws_bytes, bool need_kv, Prepared *pr, DeviceState **dst) {
+// Argument checks that need no CUDA call.
+int check_args(const mla_shape_t *sh, const void *q, const void *k_cache, const int32_t *block_table,
+               const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, const void *out,
+               const float *lse, bool need_kv) {
     int st = check_shape(sh);
     if (st != MLA_OK) return st;
     if (!cache_seqlens || !md || !num_splits || !out || !lse)
@@ -243,6 +289,14 @@ int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int
     if (need_kv && (!q || !k_cache || !block_table)) return fail(MLA_ERR_ARG, "NULL tensor pointer");
     if ((need_kv && (!aligned16(q) || !aligned16(k_cache))) || !aligned16(out))
         return fail(MLA_ERR_ARG, "q, k_cache and out must be 16-byte aligned");
+    return MLA_OK;
+}
+
+int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int32_t *block_table,
+            const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale, int causal,
+            void *out, float *lse, void *ws, size_t ws_bytes, bool need_kv, Prepared *pr, DeviceState **dst) {
+    int st = check_args(sh, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, need_kv);
+    if (st != MLA_OK) return st;
     size_t lse_off = 0;
     const size_t need = workspace_bytes_for(sh, &lse_off);
     if (!ws) return fail(MLA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
@@ -384,6 +438,11 @@ int mla_workspace_size(const mla_shape_t *shape, size_t *bytes) {
 int mla_decode_splitkv(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
                        const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
                        int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    if (!ws && ws_bytes == 0) {
+        int wst = check_args(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, true);
+        if (wst == MLA_OK) wst = internal_workspace(shape, reinterpret_cast<cudaStream_t>(stream), &ws, &ws_bytes);
+        if (wst != MLA_OK) return wst;
+    }
     Prepared pr;
     DeviceState *ds = nullptr;
     int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
@@ -396,6 +455,11 @@ int mla_decode_splitkv(const mla_shape_t *shape, const void *q, const void *k_ca
 int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
                        const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
                        int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    if (!ws && ws_bytes == 0) {
+        int wst = check_args(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, false);
+        if (wst == MLA_OK) wst = internal_workspace(shape, reinterpret_cast<cudaStream_t>(stream), &ws, &ws_bytes);
+        if (wst != MLA_OK) return wst;
+    }
     Prepared pr;
     DeviceState *ds = nullptr;
     int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
@@ -408,6 +472,11 @@ int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_ca
 int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
                    const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
                    int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    if (!ws && ws_bytes == 0) {
+        int wst = check_args(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, true);
+        if (wst == MLA_OK) wst = internal_workspace(shape, reinterpret_cast<cudaStream_t>(stream), &ws, &ws_bytes);
+        if (wst != MLA_OK) return wst;
+    }
     Prepared pr;
     DeviceState *ds = nullptr;
     int st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
@@ -418,6 +487,23 @@ int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
     st = launch_splitkv(shape, k_cache, pr, s);
     if (st != MLA_OK) return st;
     return launch_combine(shape, pr, s);
+}
+
+int mla_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    int prev = 0;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int status = MLA_OK;
+    for (auto &w : g_ws) {
+        if (!w.ptr) continue;
+        if ((e = cudaSetDevice(w.device)) == cudaSuccess && (e = cudaDeviceSynchronize()) == cudaSuccess)
+            e = cudaFree(w.ptr);
+        if (e != cudaSuccess && status == MLA_OK) status = cuda_fail(e, "mla_shutdown: freeing the internal workspace");
+        w = WsEntry();
+    }
+    cudaSetDevice(prev);
+    return status;
 }
 
 int mla_check_device_error(int *bits, int clear) {

@@ -181,3 +181,32 @@ def test_full_size_workloads_sampled_rows(name):
     assert_close(out, lse, ref_o, ref_l, rows=rows, where=name)
     import paged_mla_decode_10_gb300 as M
     assert M.mla_check_device_error(clear=True) == 0
+
+
+def test_null_workspace_uses_internal_stream_ordered_buffer():
+    """workspace NULL / 0 bytes: the library's own buffer per (device, stream),
+    on two streams and again after mla_shutdown released it."""
+    import ctypes
+    import paged_mla_decode_10_gb300 as M
+    from paged_mla_decode_10_gb300 import _lib
+    L = _lib.load()
+    inp = _custom("h128_ragged", 6, 1, 128, [1, 63, 64, 65, 200, 1000], seed=5).to("cuda")
+    w = inp.workload
+    md, ns = M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=3)   # split sequences
+    ref_o, ref_l = oracle(inp)
+    for attempt in range(2):
+        for stream in (torch.cuda.Stream(), torch.cuda.current_stream()):
+            out = torch.empty(w.batch, w.s_q, w.h_q, 512, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(w.batch, w.h_q, w.s_q, dtype=torch.float32, device="cuda")
+            sh = M.make_shape(inp.q, inp.k_cache, inp.block_table, out.stride()[:3], 3, 512)
+            stream.wait_stream(torch.cuda.current_stream())
+            rc = L.mla_decode_fwd(ctypes.byref(sh), ctypes.c_void_p(inp.q.data_ptr()),
+                                  ctypes.c_void_p(inp.k_cache.data_ptr()), ctypes.c_void_p(inp.block_table.data_ptr()),
+                                  ctypes.c_void_p(inp.cache_seqlens.data_ptr()), ctypes.c_void_p(md.data_ptr()),
+                                  ctypes.c_void_p(ns.data_ptr()), ctypes.c_float(inp.scale), 0,
+                                  ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()), None, 0,
+                                  ctypes.c_void_p(stream.cuda_stream))
+            assert rc == 0, L.mla_last_error()
+            stream.synchronize()
+            assert_close(out, lse, ref_o, ref_l, where=f"internal workspace, attempt {attempt}")
+        assert L.mla_shutdown() == 0, L.mla_last_error()
