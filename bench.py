@@ -24,6 +24,7 @@ no cross-GPU step); value is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -312,6 +313,19 @@ def run_libmla(args, w, world, rank, local):
     call_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = reduce_max(sum(call_ms) / len(call_ms), world, dev)
     clocks = clk.summary()
+    srt = sorted(call_ms)
+    pct = lambda f: 1e3 * srt[min(len(srt) - 1, int(f * (len(srt) - 1) + 0.5))]
+    dist_us = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9)}
+
+    # ---- the same call with a warm L2 (no flush between calls), labelled as such
+    evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        evw[i][0].record(stream)
+        decode()
+        evw[i][1].record(stream)
+    torch.cuda.synchronize()
+    warm_us = 1e3 * sum(a.elapsed_time(b) for a, b in evw) / args.steps
 
     # ---- roofline: the split-KV kernel and the combine kernel timed separately
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
@@ -328,14 +342,26 @@ def run_libmla(args, w, world, rank, local):
     c_ms = [b.elapsed_time(c) for _, b, c in ev3]
     kernel_ms = reduce_max(sum(k_ms) / len(k_ms), world, dev)
     combine_ms = sum(c_ms) / len(c_ms)
-    # ---- the schedule (mla_get_metadata) on its own: amortised over the layers of a step
-    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        evm[i][0].record(stream)
-        M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=parts)
-        evm[i][1].record(stream)
+    # ---- the schedule (mla_get_metadata) on its own: amortised over the layers of a step.
+    # The calls are queued behind a GPU sleep, so the interval between the two
+    # events is device time (back-to-back launches), not the host's launch latency.
+    md_buf = torch.empty_like(md)
+    ns_buf = torch.empty_like(ns)
+    L_md = M._lib.load()
+    n_md = 20
+    em0, em1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    metadata_us = 1e3 * sum(a.elapsed_time(b) for a, b in evm) / args.steps
+    torch.cuda._sleep(2_000_000)
+    em0.record(stream)
+    for _ in range(n_md):
+        M._lib.check(L_md.mla_get_metadata(ctypes.c_void_p(inp.cache_seqlens.data_ptr()), w.batch, w.rows, w.h_k, parts,
+                                           ctypes.c_void_p(md_buf.data_ptr()), ctypes.c_void_p(ns_buf.data_ptr()),
+                                           ctypes.c_void_p(stream.cuda_stream)), "mla_get_metadata")
+    em1.record(stream)
+    torch.cuda.synchronize()
+    metadata_us = 1e3 * em0.elapsed_time(em1) / n_md
+    if not (torch.equal(md_buf, md) and torch.equal(ns_buf, ns)):
+        raise RuntimeError("schedule differs between calls")
     bits = M.mla_check_device_error(clear=True)
     if bits:
         raise RuntimeError(f"device error bits {bits} during the benchmark")
@@ -413,6 +439,7 @@ def run_libmla(args, w, world, rank, local):
                      "unit": unit, "frac": achieved / peak, "traffic": traffic, "peak_source": peaks_src,
                      "kernel_us": kernel_ms * 1e3, "combine_us": combine_ms * 1e3,
                      "algorithmic_per_launch": nbytes if bound == "hbm" else flop},
+        "call_us": dict(dist_us, mean=ms_per_step * 1e3, warm_l2_mean=warm_us),
         "metadata_us": metadata_us,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

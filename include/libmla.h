@@ -128,7 +128,7 @@ int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, 
  * ceil((W + (num_sm_parts - 1) * 6) / num_sm_parts), W = sum(n_b + 6).
  * Errors: MLA_ERR_ARG (NULL pointer, batch < 0, num_sm_parts < 1,
  * num_heads_per_head_k < 1, num_heads_k < 1), MLA_ERR_UNSUPPORTED
- * (batch > 16384), MLA_ERR_CUDA.
+ * (batch > 16384 or num_sm_parts > 1024), MLA_ERR_CUDA.
  */
 int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k,
                      int num_heads_k, int num_sm_parts, int32_t *tile_scheduler_metadata,

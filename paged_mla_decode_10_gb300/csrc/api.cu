@@ -18,6 +18,7 @@ __global__ void mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, co
                                    const __grid_constant__ DecodeParams p);
 __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
 __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
+size_t metadata_smem_bytes(int batch, int parts);
 uint32_t splitkv_smem_bytes();
 uint32_t splitkv_threads();
 uint32_t combine_threads();
@@ -33,6 +34,7 @@ using namespace mla;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxBatchMetadata = 16384;
+constexpr int kMaxPartsMetadata = 1024;
 constexpr int kMaxRowsPerHead = 1024;
 
 thread_local std::string t_last_error;
@@ -86,7 +88,7 @@ int device_state(DeviceState **out) {
                 cudaSuccess)
                 return cuda_fail(e, "cudaFuncSetAttribute(splitkv)");
             if ((e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          2 * kMaxBatchMetadata * 4)) != cudaSuccess)
+                                          (int)metadata_smem_bytes(kMaxBatchMetadata, kMaxPartsMetadata))) != cudaSuccess)
                 return cuda_fail(e, "cudaFuncSetAttribute(metadata)");
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 64, 1, 1);
@@ -416,10 +418,12 @@ int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_
     if (batch < 0 || num_sm_parts < 1 || num_heads_per_head_k < 1 || num_heads_k < 1)
         return fail(MLA_ERR_ARG, "mla_get_metadata: bad argument");
     if (batch > kMaxBatchMetadata) return fail(MLA_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatchMetadata);
+    if (num_sm_parts > kMaxPartsMetadata)
+        return fail(MLA_ERR_UNSUPPORTED, "num_sm_parts %d > %d", num_sm_parts, kMaxPartsMetadata);
     DeviceState *ds = nullptr;
     int st = device_state(&ds);
     if (st != MLA_OK) return st;
-    const size_t smem = (size_t)2 * (batch > 0 ? batch : 1) * sizeof(int32_t);
+    const size_t smem = metadata_smem_bytes(batch, num_sm_parts);
     mla_metadata_kernel<<<1, 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
         cache_seqlens, batch, num_sm_parts, tile_scheduler_metadata, num_splits);
     cudaError_t e = cudaGetLastError();

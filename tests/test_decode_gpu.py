@@ -91,6 +91,27 @@ def test_metadata_bit_exact_on_random_small_cases():
         np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
 
 
+def test_metadata_bit_exact_at_the_size_limits():
+    """Largest batch and part count the schedule kernel takes, parts spanning
+    hundreds of sequences (the walk's multi-window search), and the refusal
+    one part past the limit."""
+    import paged_mla_decode_10_gb300 as M
+    rng = np.random.default_rng(12)
+    cases = [(rng.integers(0, 20000, 16384), 1024), (rng.integers(0, 20000, 16384), 76),
+             (rng.integers(0, 100, 5000), 7), (np.full(16384, 64), 1), (np.zeros(16384, dtype=np.int64), 1024)]
+    for L, parts in cases:
+        Ls = [int(x) for x in L]
+        Lt = torch.tensor(Ls, dtype=torch.int32, device="cuda")
+        md, ns = M.mla_get_metadata(Lt, 128, 1, num_sm_parts=parts)
+        md_ref, ns_ref = OM.schedule(Ls, parts)
+        np.testing.assert_array_equal(md.cpu().numpy(), md_ref, err_msg=f"B={len(Ls)} parts={parts}")
+        np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
+    with pytest.raises(M.MlaError):
+        M.mla_get_metadata(torch.ones(4, dtype=torch.int32, device="cuda"), 128, 1, num_sm_parts=1025)
+    with pytest.raises(M.MlaError):
+        M.mla_get_metadata(torch.ones(16385, dtype=torch.int32, device="cuda"), 128, 1, num_sm_parts=4)
+
+
 def test_num_sm_parts_variation_consistent():
     inp = _custom("parts", 4, 1, 128, [3000, 100, 64, 2049], seed=9)
     ref_o, ref_l = oracle(inp)
