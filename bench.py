@@ -10,10 +10,11 @@ write) before every timed call.  Prints ONE JSON line.
              resident in HBM, mean over the timed calls, max over ranks
   roofline   the split-KV decode kernel alone: algorithmic bytes (or FLOPs)
              of one launch / its mean CUDA-event duration vs the measured peak
-  e2e        the same call through the public API with host (pinned) buffers:
-             H2D of q, block_table, cache_seqlens, the schedule, the decode,
-             D2H of out and softmax_lse, all inside the timed region (the KV
-             cache is model state and stays resident)
+  e2e        one mla_decode_fwd_host call per step (the C ABI's host-buffer
+             entry) with page-locked host buffers: H2D of q, block_table and
+             cache_seqlens, the schedule, the decode, and out / softmax_lse
+             back in host memory, all inside the timed region (the KV cache is
+             model state and stays resident)
   cpu_baseline  the fp64 C oracle on the host cores, on a bounded sample of
              the same workload, scaled to us per call by FLOPs
 
@@ -377,23 +378,16 @@ def run_libmla(args, w, world, rank, local):
         peak, unit = peaks["bf16_tflops"], "TFLOP/s"
     traffic = recorded_traffic(w.name)
 
-    # ---- e2e through the public API with host buffers
+    # ---- e2e: one host-buffer call per step (copies in, schedule, decode, results back in host memory)
     q_h = inp.q.cpu().pin_memory()
     bt_h = inp.block_table.cpu().pin_memory()
     L_h = inp.cache_seqlens.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, bt_d, L_d = torch.empty_like(inp.q), torch.empty_like(inp.block_table), torch.empty_like(inp.cache_seqlens)
 
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        L_d.copy_(L_h, non_blocking=True)
-        md2, ns2 = M.mla_get_metadata(L_d, w.rows, w.h_k, num_sm_parts=parts)
-        M.mla_decode_fwd(q_d, inp.k_cache, bt_d, L_d, 512, md2, ns2, softmax_scale=inp.scale, causal=w.causal,
-                         out=out, softmax_lse=lse, workspace=ws)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        M.mla_decode_fwd_host(q_h, inp.k_cache, bt_h, L_h, 512, softmax_scale=inp.scale, causal=w.causal,
+                              num_sm_parts=parts, out=out_h, softmax_lse=lse_h)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -406,6 +400,8 @@ def run_libmla(args, w, world, rank, local):
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev2) / args.steps, world, dev)
+    if not (torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())):
+        raise RuntimeError("the host-buffer call returned a different result from the device call")
     h2d = q_h.numel() * 2 + bt_h.numel() * 4 + L_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 

@@ -16,9 +16,11 @@
  *                        softmax_lse (batch, h_q, s_q)
  *
  * Conventions shared by every call
- *   - Every tensor argument is a plain device pointer owned by the caller;
- *     libmla keeps no reference to it after the call returns.  Nothing is
- *     allocated by libmla on any call.
+ *   - Every tensor argument is a plain pointer owned by the caller (device
+ *     memory, except the host buffers of mla_decode_fwd_host); libmla keeps
+ *     no reference to it after the call returns.  libmla allocates device
+ *     memory only for calls that pass no workspace and for
+ *     mla_decode_fwd_host (stream-ordered, released by mla_shutdown).
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and runs asynchronously; no call synchronizes the host
  *     except mla_check_device_error.
@@ -232,8 +234,48 @@ int mla_decode_fwd_noalloc(const mla_shape_t *shape, const void *q, const void *
                            mla_stream_t stream);
 
 /*
+ * One whole decode step from host buffers: copies q, block_table and
+ * cache_seqlens to the device, computes the schedule (mla_get_metadata with
+ * shape->num_sm_parts parts), decodes (mla_decode_fwd) and returns out and
+ * softmax_lse to host memory, all enqueued on `stream` -- the sequence of the
+ * FlashMLA-PyTorch page's usage (get_mla_metadata from cache_seqlens, then
+ * flash_mla_with_kvcache) with the host transfers around it.  The results are in
+ * the host buffers once `stream` has completed; the inputs must stay
+ * unchanged until then.
+ *   q_host              host, bf16, laid out by shape->q_stride
+ *   block_table_host    host, int32, row stride shape->bt_stride
+ *   cache_seqlens_host  host, int32, batch entries
+ *   k_cache             DEVICE (the cache stays resident), as mla_decode_fwd
+ *   out_host            host, bf16 (batch, s_q, h_q, 512), contiguous:
+ *                       shape->out_stride must be {s_q*h_q*512, h_q*512, 512}
+ *   softmax_lse_host    host, fp32 (batch, h_q, s_q), contiguous
+ * Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister) for
+ * the copies to be asynchronous; pageable memory works, with copies that
+ * block the host.  When out_host / softmax_lse_host are page-locked and
+ * mapped into the device's address space, the kernels store the results
+ * there directly and no device-to-host copy is made; otherwise they are
+ * staged in device memory and copied back.  The schedule runs on a second,
+ * library-owned stream while q is copied, and `stream` waits for it before
+ * the decode, so work enqueued on `stream` afterwards is ordered after the
+ * whole step.
+ * Device staging (inputs, schedule, workspace, output staging) is one
+ * buffer per (device, stream), allocated and grown with cudaMallocAsync on
+ * `stream`, and released, with the second stream, by mla_shutdown.
+ * batch == 0 enqueues nothing (the pointers may then be NULL).
+ * Errors: as mla_decode_fwd and mla_get_metadata (MLA_ERR_UNSUPPORTED for
+ * batch > 16384 or num_sm_parts > 1024), plus MLA_ERR_ARG for a
+ * non-contiguous out.  A CUDA failure after the first copy was enqueued
+ * returns MLA_ERR_CUDA with part of the step enqueued.
+ */
+int mla_decode_fwd_host(const mla_shape_t *shape, const void *q_host, const void *k_cache,
+                        const int32_t *block_table_host, const int32_t *cache_seqlens_host,
+                        float softmax_scale, int causal, void *out_host, float *softmax_lse_host,
+                        mla_stream_t stream);
+
+/*
  * Releases the internal workspaces that calls without a workspace allocated
- * (synchronizing each device that holds one first).  Later such calls
+ * and the staging buffers and streams of mla_decode_fwd_host (synchronizing
+ * each device that holds one first).  Later such calls
  * allocate again.  Not to be called while another thread uses the library.
  * Errors: MLA_ERR_CUDA.
  */

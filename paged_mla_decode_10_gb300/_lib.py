@@ -1,6 +1,6 @@
 """ctypes binding of libmla.so (argument marshalling only).
 
-Every function here forwards raw device pointers and sizes to the C ABI in
+Every function here forwards raw pointers and sizes to the C ABI in
 include/libmla.h; all computation happens in the library's CUDA kernels.
 There is no fallback: if libmla.so is missing or cannot be loaded, importing
 the package raises.
@@ -76,6 +76,8 @@ def load():
         getattr(L, name).restype = c_int
     L.mla_decode_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
     L.mla_decode_fwd_noalloc.restype = c_int
+    L.mla_decode_fwd_host.argtypes = [sp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
+    L.mla_decode_fwd_host.restype = c_int
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]
     L.mla_shutdown.argtypes = []
     L.mla_shutdown.restype = c_int

@@ -153,6 +153,42 @@ def mla_decode_combine(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_
                         workspace, stream)
 
 
+def mla_decode_fwd_host(q, k_cache, block_table, cache_seqlens, head_dim_v, softmax_scale=None, causal=False,
+                        num_sm_parts=None, out=None, softmax_lse=None, stream=None):
+    """One decode step from host tensors: q, block_table, cache_seqlens and the results live in host
+    memory (pin them for asynchronous copies), k_cache on the device.  The schedule, the copies and
+    the decode are enqueued on `stream`; the results are valid once it has completed.
+    Returns (out (B, s_q, h_q, head_dim_v) bf16, softmax_lse (B, h_q, s_q) fp32), both host tensors."""
+    L = _lib.load()
+    _require(q.dim() == 4 and k_cache.dim() == 4, "q and k_cache must be 4-D")
+    _require(q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16, "q and k_cache must be bf16")
+    _require(block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32,
+             "block_table and cache_seqlens must be int32")
+    _require(k_cache.is_cuda, "k_cache must be a CUDA tensor")
+    _require(not any(t.is_cuda for t in (q, block_table, cache_seqlens)), "q, block_table, cache_seqlens: host tensors")
+    _require(cache_seqlens.dim() == 1 and cache_seqlens.is_contiguous(), "cache_seqlens: contiguous 1-D")
+    _require(block_table.stride(1) == 1 and q.stride(3) == 1, "last dimensions must be contiguous")
+    B, s_q, h_q, _ = q.shape
+    h_k = k_cache.shape[2]
+    if softmax_scale is None:
+        softmax_scale = q.shape[-1] ** (-0.5)
+    if num_sm_parts is None:
+        num_sm_parts = mla_get_num_sm_parts(s_q * h_q // h_k, h_k, k_cache.device)
+    pin = torch.cuda.is_available()
+    if out is None:
+        out = torch.empty((B, s_q, h_q, head_dim_v), dtype=torch.bfloat16, pin_memory=pin)
+    if softmax_lse is None:
+        softmax_lse = torch.empty((B, h_q, s_q), dtype=torch.float32, pin_memory=pin)
+    _require(not out.is_cuda and out.is_contiguous(), "out: contiguous host tensor")
+    _require(not softmax_lse.is_cuda and softmax_lse.is_contiguous() and softmax_lse.dtype == torch.float32,
+             "softmax_lse: contiguous fp32 host tensor")
+    sh = make_shape(q, k_cache, block_table, out.stride()[:3], num_sm_parts, head_dim_v)
+    check(L.mla_decode_fwd_host(ctypes.byref(sh), _ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(cache_seqlens),
+                                float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(softmax_lse),
+                                _stream(stream)), "mla_decode_fwd_host")
+    return out, softmax_lse
+
+
 def mla_check_device_error(clear: bool = True) -> int:
     """Synchronize and return the MLA_DEVERR_* bits kernels raised (cleared if asked)."""
     L = _lib.load()
@@ -162,7 +198,8 @@ def mla_check_device_error(clear: bool = True) -> int:
 
 
 def mla_shutdown() -> None:
-    """Release the library's internal workspaces (those of calls made with workspace=NULL)."""
+    """Release the library's internal workspaces (calls made with workspace=NULL) and the
+    staging buffers of mla_decode_fwd_host."""
     L = _lib.load()
     check(L.mla_shutdown(), "mla_shutdown")
 

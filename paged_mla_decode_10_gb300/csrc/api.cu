@@ -367,6 +367,113 @@ int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t strea
     return MLA_OK;
 }
 
+int launch_metadata(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits,
+                    cudaStream_t stream) {
+    mla_metadata_kernel<<<1, 256, metadata_smem_bytes(batch, parts), stream>>>(seqlens, batch, parts, md, num_splits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "metadata launch");
+    return MLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// the host-buffer path (mla_decode_fwd_host)
+// ---------------------------------------------------------------------------
+// Device staging for one (device, stream): the workspace, the inputs copied
+// from the host, the schedule, and output staging for host buffers the
+// kernels cannot write directly.  Grown with cudaMallocAsync / cudaFreeAsync
+// on the stream.  `side` is a second stream on which the schedule is
+// computed while q is copied; `fork` / `join` order it against `stream`.
+struct HostEntry {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+constexpr int kHostEntries = 16;
+HostEntry g_host[kHostEntries];   // guarded by g_ws_mu
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Staging areas, in order: workspace, q, block_table, cache_seqlens,
+// metadata, num_splits, out, lse (each 256-byte aligned).
+enum { kStWs, kStQ, kStBt, kStLen, kStMd, kStNs, kStOut, kStLse, kStCount };
+struct HostLayout {
+    size_t off[kStCount], size[kStCount], total;
+};
+
+HostLayout host_layout(const mla_shape_t *sh) {
+    const int64_t B = sh->batch;
+    HostLayout l;
+    l.size[kStWs] = workspace_bytes_for(sh, nullptr);
+    l.size[kStQ] = B > 0 ? (size_t)((B - 1) * sh->q_stride[0] + (sh->s_q - 1) * sh->q_stride[1] +
+                                    (sh->h_q - 1) * sh->q_stride[2] + sh->head_dim) * 2
+                         : 0;
+    l.size[kStBt] = B > 0 ? (size_t)((B - 1) * sh->bt_stride + sh->max_blocks_per_seq) * 4 : 0;
+    l.size[kStLen] = (size_t)B * 4;
+    l.size[kStMd] = (size_t)sh->num_sm_parts * MLA_METADATA_SIZE * 4;
+    l.size[kStNs] = (size_t)(B + 1) * 4;
+    l.size[kStOut] = (size_t)B * sh->s_q * sh->h_q * MLA_HEAD_DIM_V * 2;
+    l.size[kStLse] = (size_t)B * sh->h_q * sh->s_q * 4;
+    size_t o = 0;
+    for (int i = 0; i < kStCount; ++i) {
+        l.off[i] = o;
+        o += align256(l.size[i]);
+    }
+    l.total = o;
+    return l;
+}
+
+int host_entry(cudaStream_t stream, size_t need, HostEntry **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    HostEntry *slot = nullptr;
+    for (auto &h : g_host) {
+        if (h.side && h.device == dev && h.stream == stream) { slot = &h; break; }
+        if (!h.side && !slot) slot = &h;
+    }
+    if (!slot) return fail(MLA_ERR_UNSUPPORTED, "more than %d (device, stream) pairs use the host-buffer path", kHostEntries);
+    if (!slot->side) {
+        if ((e = cudaStreamCreateWithFlags(&slot->side, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreateWithFlags");
+        if ((e = cudaEventCreateWithFlags(&slot->fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&slot->join, cudaEventDisableTiming)) != cudaSuccess) {
+            if (slot->fork) cudaEventDestroy(slot->fork);
+            cudaStreamDestroy(slot->side);
+            *slot = HostEntry();
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
+        slot->device = dev;
+        slot->stream = stream;
+    }
+    if (slot->bytes < need) {
+        if (slot->ptr && (e = cudaFreeAsync(slot->ptr, stream)) != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(staging)");
+        slot->ptr = nullptr;
+        slot->bytes = 0;
+        void *ptr = nullptr;
+        if ((e = cudaMallocAsync(&ptr, need, stream)) != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(staging)");
+        slot->ptr = ptr;
+        slot->bytes = need;
+    }
+    *out = slot;
+    return MLA_OK;
+}
+
+// The device address the kernels may write for host buffer `h`: its mapped
+// alias when `h` is page-locked memory mapped into the device's address
+// space, else NULL (the result is staged and copied back).
+void *mapped_alias(void *h) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 }  // namespace
 
 namespace mla {
@@ -423,12 +530,8 @@ int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_
     DeviceState *ds = nullptr;
     int st = device_state(&ds);
     if (st != MLA_OK) return st;
-    const size_t smem = metadata_smem_bytes(batch, num_sm_parts);
-    mla_metadata_kernel<<<1, 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-        cache_seqlens, batch, num_sm_parts, tile_scheduler_metadata, num_splits);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "metadata launch");
-    return MLA_OK;
+    return launch_metadata(cache_seqlens, batch, num_sm_parts, tile_scheduler_metadata, num_splits,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_workspace_size(const mla_shape_t *shape, size_t *bytes) {
@@ -493,6 +596,68 @@ int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
     return launch_combine(shape, pr, s);
 }
 
+int mla_decode_fwd_host(const mla_shape_t *shape, const void *q_host, const void *k_cache,
+                        const int32_t *block_table_host, const int32_t *cache_seqlens_host, float scale, int causal,
+                        void *out_host, float *lse_host, mla_stream_t stream) {
+    int st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    const mla_shape_t &sh = *shape;
+    if (sh.batch == 0) return MLA_OK;   // nothing to compute; the pointers of empty tensors may be NULL
+    if (!q_host || !k_cache || !block_table_host || !cache_seqlens_host || !out_host || !lse_host)
+        return fail(MLA_ERR_ARG, "NULL pointer");
+    if (!aligned16(q_host) || !aligned16(k_cache) || !aligned16(out_host))
+        return fail(MLA_ERR_ARG, "q, k_cache and out must be 16-byte aligned");
+    const int64_t o2 = MLA_HEAD_DIM_V, o1 = (int64_t)sh.h_q * o2, o0 = (int64_t)sh.s_q * o1;
+    if (sh.out_stride[0] != o0 || sh.out_stride[1] != o1 || sh.out_stride[2] != o2)
+        return fail(MLA_ERR_ARG, "out must be contiguous for the host-buffer call");
+    if (sh.batch > kMaxBatchMetadata) return fail(MLA_ERR_UNSUPPORTED, "batch %d > %d", sh.batch, kMaxBatchMetadata);
+    if (sh.num_sm_parts > kMaxPartsMetadata)
+        return fail(MLA_ERR_UNSUPPORTED, "num_sm_parts %d > %d", sh.num_sm_parts, kMaxPartsMetadata);
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MLA_OK) return st;
+
+    const HostLayout lay = host_layout(&sh);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    HostEntry *h = nullptr;
+    if ((st = host_entry(s, lay.total, &h)) != MLA_OK) return st;
+    char *base = static_cast<char *>(h->ptr);
+    void *ws = base + lay.off[kStWs];
+    void *q_d = base + lay.off[kStQ];
+    int32_t *bt_d = reinterpret_cast<int32_t *>(base + lay.off[kStBt]);
+    int32_t *L_d = reinterpret_cast<int32_t *>(base + lay.off[kStLen]);
+    int32_t *md_d = reinterpret_cast<int32_t *>(base + lay.off[kStMd]);
+    int32_t *ns_d = reinterpret_cast<int32_t *>(base + lay.off[kStNs]);
+    void *out_direct = mapped_alias(out_host);
+    void *lse_direct = mapped_alias(lse_host);
+    void *out_d = out_direct ? out_direct : base + lay.off[kStOut];
+    float *lse_d = static_cast<float *>(lse_direct ? lse_direct : base + lay.off[kStLse]);
+
+    Prepared pr;
+    if ((st = prepare(&sh, q_d, k_cache, bt_d, L_d, md_d, ns_d, scale, causal, out_d, lse_d, ws, lay.size[kStWs], true,
+                      &pr, &ds)) != MLA_OK)
+        return st;
+    cudaError_t e;
+    // schedule stream: cache_seqlens and block_table in, then the schedule
+    if ((e = cudaEventRecord(h->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(h->side, h->fork, 0)) != cudaSuccess)
+        return cuda_fail(e, "fork to the schedule stream");
+    if ((e = cudaMemcpyAsync(L_d, cache_seqlens_host, lay.size[kStLen], cudaMemcpyHostToDevice, h->side)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(bt_d, block_table_host, lay.size[kStBt], cudaMemcpyHostToDevice, h->side)) != cudaSuccess)
+        return cuda_fail(e, "copy of cache_seqlens / block_table");
+    if ((st = launch_metadata(L_d, sh.batch, sh.num_sm_parts, md_d, ns_d, h->side)) != MLA_OK) return st;
+    if ((e = cudaEventRecord(h->join, h->side)) != cudaSuccess) return cuda_fail(e, "join event");
+    // this stream: q in, wait for the schedule, decode, results out
+    if ((e = cudaMemcpyAsync(q_d, q_host, lay.size[kStQ], cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "copy of q");
+    if ((e = cudaStreamWaitEvent(s, h->join, 0)) != cudaSuccess) return cuda_fail(e, "join of the schedule stream");
+    if ((st = launch_splitkv(&sh, k_cache, pr, s)) != MLA_OK) return st;
+    if ((st = launch_combine(&sh, pr, s)) != MLA_OK) return st;
+    if (!out_direct && (e = cudaMemcpyAsync(out_host, out_d, lay.size[kStOut], cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "copy of out");
+    if (!lse_direct && (e = cudaMemcpyAsync(lse_host, lse_d, lay.size[kStLse], cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "copy of softmax_lse");
+    return MLA_OK;
+}
+
 int mla_shutdown(void) {
     std::lock_guard<std::mutex> lock(g_ws_mu);
     int prev = 0;
@@ -505,6 +670,17 @@ int mla_shutdown(void) {
             e = cudaFree(w.ptr);
         if (e != cudaSuccess && status == MLA_OK) status = cuda_fail(e, "mla_shutdown: freeing the internal workspace");
         w = WsEntry();
+    }
+    for (auto &h : g_host) {
+        if (!h.side) continue;
+        if ((e = cudaSetDevice(h.device)) == cudaSuccess && (e = cudaDeviceSynchronize()) == cudaSuccess) {
+            if (h.ptr) e = cudaFree(h.ptr);
+            cudaEventDestroy(h.fork);
+            cudaEventDestroy(h.join);
+            cudaStreamDestroy(h.side);
+        }
+        if (e != cudaSuccess && status == MLA_OK) status = cuda_fail(e, "mla_shutdown: releasing the host-path staging");
+        h = HostEntry();
     }
     cudaSetDevice(prev);
     return status;

@@ -88,3 +88,16 @@ def test_metadata_rejects_bad_arguments(lib):
     dummy = ctypes.c_void_p(256)
     assert lib.mla_get_metadata(dummy, -1, 128, 1, 76, dummy, dummy, None) == 1
     assert lib.mla_get_metadata(dummy, 4, 128, 1, 0, dummy, dummy, None) == 1
+
+
+def test_host_decode_rejects_bad_arguments_before_any_cuda_call(lib):
+    dummy = ctypes.c_void_p(256)
+    sh = _shape()
+    args = lambda s, q=dummy, out=dummy: (ctypes.byref(s), q, dummy, dummy, dummy, ctypes.c_float(0.0), 0, out,
+                                          dummy, None)
+    assert lib.mla_decode_fwd_host(*args(sh, q=None)) == 1                                # NULL q
+    assert lib.mla_decode_fwd_host(*args(sh, out=ctypes.c_void_p(264))) == 1              # out not 16-byte aligned
+    assert lib.mla_decode_fwd_host(*args(_shape(out_stride=(32 * 512, 16 * 512, 512)))) == 1   # out not contiguous
+    assert b"contiguous" in lib.mla_last_error()
+    assert lib.mla_decode_fwd_host(*args(_shape(num_sm_parts=1025))) == 2                 # schedule limit
+    assert lib.mla_decode_fwd_host(*args(_shape(head_dim=512))) == 1                      # bad shape
