@@ -184,6 +184,10 @@ def oracle_sample(inp_cpu, target_flop, seed=0):
     return sorted(rows), flop
 
 
+# Workloads up to this many FLOPs also get a whole-call single-thread oracle time.
+SINGLE_THREAD_FLOP = 1e9
+
+
 def time_oracle(inp_cpu, rows, threads=0):
     from oracle import reference as R
     t0 = time.perf_counter()
@@ -416,6 +420,9 @@ def run_libmla(args, w, world, rank, local):
         cpu = {"value": t * (flop / sflop) * 1e6, "unit": UNIT, "cores": R.max_threads(), "kind": "oracle",
                "sample": f"{len(rows)} of {w.batch * w.s_q * w.h_q} query rows ({sflop / 1e9:.2f} of "
                          f"{flop / 1e9:.1f} GFLOP, {t:.1f} s), scaled to one call by FLOPs"}
+        if flop <= SINGLE_THREAD_FLOP:
+            # a workload small enough for one core: the whole call, single-threaded
+            cpu["single_thread_us"] = time_oracle(inp_cpu, None, threads=1) * 1e6
 
     if rank != 0:
         return 0
