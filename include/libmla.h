@@ -234,6 +234,38 @@ int mla_decode_fwd_noalloc(const mla_shape_t *shape, const void *q, const void *
                            mla_stream_t stream);
 
 /*
+ * Strides (elements) of the RoPE tensors of mla_decode_fwd_split.
+ */
+typedef struct {
+    int64_t q_rope_stride[3];   /* q_rope (batch, s_q, h_q, 64): {batch, token, head}            */
+    int64_t krope_stride[3];    /* krope (num_blocks, 64, h_k, 64): {block, row, kv-head}          */
+} mla_rope_strides_t;
+
+/*
+ * mla_decode_fwd on split inputs: the latent and RoPE parts of the query and
+ * of the cache in separate tensors, the layout of the Ascend ATB MLA page
+ * (parameter table: qNope, qRope, ctKV, kRope; cacheMode 1, separate
+ * caches).  The result is that of mla_decode_fwd on the concatenations
+ * q = [q_nope | q_rope] and k_cache = [ctkv | krope] along the last
+ * dimension; V is ctkv.
+ *   q_nope  (batch, s_q, h_q, 512) bf16   strides shape->q_stride
+ *   q_rope  (batch, s_q, h_q, 64) bf16    strides rope->q_rope_stride
+ *   ctkv    (num_blocks, 64, h_k, 512) bf16  strides shape->k_stride
+ *   krope   (num_blocks, 64, h_k, 64) bf16   strides rope->krope_stride
+ * shape->head_dim stays 576 (the logical q . k length).  Every pointer
+ * 16-byte aligned, every stride a positive multiple of 8 elements, head
+ * strides at least the head's dims.  Everything else (schedule, workspace,
+ * errors, the two launches) as mla_decode_fwd.  Both calls read the same
+ * bytes from HBM for the same problem.
+ */
+int mla_decode_fwd_split(const mla_shape_t *shape, const mla_rope_strides_t *rope,
+                         const void *q_nope, const void *q_rope, const void *ctkv, const void *krope,
+                         const int32_t *block_table, const int32_t *cache_seqlens,
+                         const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                         float softmax_scale, int causal, void *out, float *softmax_lse,
+                         void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * One whole decode step from host buffers: copies q, block_table and
  * cache_seqlens to the device, computes the schedule (mla_get_metadata with
  * shape->num_sm_parts parts), decodes (mla_decode_fwd) and returns out and

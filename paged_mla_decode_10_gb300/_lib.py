@@ -39,6 +39,10 @@ class MlaShape(ctypes.Structure):
     ]
 
 
+class MlaRopeStrides(ctypes.Structure):
+    _fields_ = [("q_rope_stride", ctypes.c_int64 * 3), ("krope_stride", ctypes.c_int64 * 3)]
+
+
 class MlaError(RuntimeError):
     def __init__(self, status: int, func: str, detail: str):
         self.status = status
@@ -76,6 +80,9 @@ def load():
         getattr(L, name).restype = c_int
     L.mla_decode_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
     L.mla_decode_fwd_noalloc.restype = c_int
+    L.mla_decode_fwd_split.argtypes = [sp, ctypes.POINTER(MlaRopeStrides), vp, vp, vp, vp, vp, vp, vp, vp,
+                                       ctypes.c_float, c_int, vp, vp, vp, c_size, vp]
+    L.mla_decode_fwd_split.restype = c_int
     L.mla_decode_fwd_host.argtypes = [sp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
     L.mla_decode_fwd_host.restype = c_int
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]

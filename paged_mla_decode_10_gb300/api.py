@@ -153,6 +153,49 @@ def mla_decode_combine(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_
                         workspace, stream)
 
 
+def mla_decode_fwd_split(q_nope, q_rope, ctkv, krope, block_table, cache_seqlens, head_dim_v,
+                         tile_scheduler_metadata, num_splits, softmax_scale=None, causal=False, out=None,
+                         softmax_lse=None, workspace=None, stream=None):
+    """mla_decode_fwd on split inputs: q_nope (B, s_q, h_q, 512), q_rope (B, s_q, h_q, 64),
+    ctkv (num_blocks, 64, h_k, 512), krope (num_blocks, 64, h_k, 64), all bf16 CUDA tensors with a
+    contiguous last dimension.  Same result as mla_decode_fwd on the concatenations."""
+    L = _lib.load()
+    _require(q_nope.dim() == 4 and q_rope.dim() == 4 and ctkv.dim() == 4 and krope.dim() == 4,
+             "q_nope, q_rope, ctkv, krope must be 4-D")
+    _require(all(t.dtype == torch.bfloat16 and t.is_cuda for t in (q_nope, q_rope, ctkv, krope)),
+             "q_nope, q_rope, ctkv, krope must be bf16 CUDA tensors")
+    _require(q_nope.shape[:3] == q_rope.shape[:3] and ctkv.shape[:3] == krope.shape[:3],
+             "nope and rope parts must agree in their leading dimensions")
+    _require(q_nope.shape[3] == HEAD_DIM_V and ctkv.shape[3] == HEAD_DIM_V and q_rope.shape[3] == HEAD_DIM - HEAD_DIM_V
+             and krope.shape[3] == HEAD_DIM - HEAD_DIM_V, "last dimensions must be 512 (nope) and 64 (rope)")
+    _require(block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32,
+             "block_table and cache_seqlens must be int32")
+    B, s_q, h_q, _ = q_nope.shape
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** (-0.5)
+    if out is None:
+        out = torch.empty((B, s_q, h_q, head_dim_v), dtype=q_nope.dtype, device=q_nope.device)
+    if softmax_lse is None:
+        softmax_lse = torch.empty((B, h_q, s_q), dtype=torch.float32, device=q_nope.device)
+    _require(softmax_lse.is_contiguous() and softmax_lse.dtype == torch.float32, "softmax_lse: contiguous fp32")
+    cache_seqlens = cache_seqlens.contiguous()
+    sh = make_shape(q_nope, ctkv, block_table, out.stride()[:3], tile_scheduler_metadata.shape[0], head_dim_v)
+    sh.head_dim = HEAD_DIM
+    rs = _lib.MlaRopeStrides()
+    for i in range(3):
+        rs.q_rope_stride[i] = q_rope.stride(i)
+        rs.krope_stride[i] = krope.stride(i)
+    need = mla_workspace_size(sh)
+    if workspace is None:
+        workspace = _workspace(need, q_nope.device)
+    check(L.mla_decode_fwd_split(ctypes.byref(sh), ctypes.byref(rs), _ptr(q_nope), _ptr(q_rope), _ptr(ctkv),
+                                 _ptr(krope), _ptr(block_table), _ptr(cache_seqlens), _ptr(tile_scheduler_metadata),
+                                 _ptr(num_splits), float(softmax_scale), int(bool(causal)), _ptr(out),
+                                 _ptr(softmax_lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "mla_decode_fwd_split")
+    return out, softmax_lse
+
+
 def mla_decode_fwd_host(q, k_cache, block_table, cache_seqlens, head_dim_v, softmax_scale=None, causal=False,
                         num_sm_parts=None, out=None, softmax_lse=None, stream=None):
     """One decode step from host tensors: q, block_table, cache_seqlens and the results live in host

@@ -122,10 +122,31 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Where the cache rows come from: the latent dims (TMA boxes of 64 dims) and
+// the RoPE dims (a box of 32), either one tensor of 576-dim rows or two
+// tensors (512 and 64 dims).  Strides in elements: {block, row, kv-head}.
+struct KvSource {
+    const void *latent;
+    int64_t lat_stride[3];
+    int lat_dims;              // extent of the latent tensor's last dimension (576 or 512)
+    const void *rope;          // base of the RoPE tensor (the cache itself when rows are concatenated)
+    int64_t rope_stride[3];
+    int rope_dims;             // extent of the RoPE tensor's last dimension (576 or 64)
+};
+
+// A cache of 576-dim rows: both maps span the whole row; the RoPE boxes start
+// at dim 512 (DecodeParams::rope_x0).
+KvSource concat_source(const mla_shape_t *sh, const void *k_cache) {
+    KvSource k;
+    k.latent = k.rope = k_cache;
+    for (int i = 0; i < 3; ++i) k.lat_stride[i] = k.rope_stride[i] = sh->k_stride[i];
+    k.lat_dims = k.rope_dims = sh->head_dim;
+    return k;
+}
+
 struct MapEntry {
-    const void *ptr = nullptr;
+    KvSource src;
     int device = -1, num_blocks = 0, h_k = 0;
-    int64_t s0 = 0, s1 = 0, s2 = 0;
     CUtensorMap m128, m64;
     bool valid = false;
 };
@@ -147,13 +168,20 @@ int get_encoder(EncodeTiledFn *fn) {
     return MLA_OK;
 }
 
-int kcache_maps(const mla_shape_t *sh, const void *k_cache, CUtensorMap *m128, CUtensorMap *m64) {
+bool same_source(const KvSource &a, const KvSource &b) {
+    return a.latent == b.latent && a.rope == b.rope && a.lat_dims == b.lat_dims && a.rope_dims == b.rope_dims &&
+           !memcmp(a.lat_stride, b.lat_stride, sizeof a.lat_stride) &&
+           !memcmp(a.rope_stride, b.rope_stride, sizeof a.rope_stride);
+}
+
+// Tensor maps {dims, h_k, 64 rows, num_blocks} over the latent and the RoPE
+// dims of the cache, cached per (device, source, geometry).
+int kcache_maps(const mla_shape_t *sh, const KvSource &src, CUtensorMap *m128, CUtensorMap *m64) {
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(g_mu);
     for (auto &e : g_maps) {
-        if (e.valid && e.ptr == k_cache && e.device == dev && e.num_blocks == sh->num_blocks && e.h_k == sh->h_k &&
-            e.s0 == sh->k_stride[0] && e.s1 == sh->k_stride[1] && e.s2 == sh->k_stride[2]) {
+        if (e.valid && e.device == dev && e.num_blocks == sh->num_blocks && e.h_k == sh->h_k && same_source(e.src, src)) {
             *m128 = e.m128;
             *m64 = e.m64;
             return MLA_OK;
@@ -162,26 +190,31 @@ int kcache_maps(const mla_shape_t *sh, const void *k_cache, CUtensorMap *m128, C
     EncodeTiledFn enc;
     int st = get_encoder(&enc);
     if (st != MLA_OK) return st;
-    // dims (innermost first): head dim, kv head, row in block, block
-    const cuuint64_t gdim[4] = {(cuuint64_t)sh->head_dim, (cuuint64_t)sh->h_k, (cuuint64_t)sh->page_block_size,
-                                (cuuint64_t)sh->num_blocks};
-    const cuuint64_t gstr[3] = {(cuuint64_t)sh->k_stride[2] * 2, (cuuint64_t)sh->k_stride[1] * 2,
-                                (cuuint64_t)sh->k_stride[0] * 2};
+    const cuuint64_t gdim_l[4] = {(cuuint64_t)src.lat_dims, (cuuint64_t)sh->h_k, (cuuint64_t)sh->page_block_size,
+                                  (cuuint64_t)sh->num_blocks};
+    const cuuint64_t gdim_r[4] = {(cuuint64_t)src.rope_dims, (cuuint64_t)sh->h_k, (cuuint64_t)sh->page_block_size,
+                                  (cuuint64_t)sh->num_blocks};
+    const cuuint64_t gstr_l[3] = {(cuuint64_t)src.lat_stride[2] * 2, (cuuint64_t)src.lat_stride[1] * 2,
+                                  (cuuint64_t)src.lat_stride[0] * 2};
+    const cuuint64_t gstr_r[3] = {(cuuint64_t)src.rope_stride[2] * 2, (cuuint64_t)src.rope_stride[1] * 2,
+                                  (cuuint64_t)src.rope_stride[0] * 2};
     const cuuint32_t box128[4] = {64, 1, 64, 1}, box64[4] = {32, 1, 64, 1}, es[4] = {1, 1, 1, 1};
     MapEntry &e = g_maps[g_map_next];
-    CUresult r1 = enc(&e.m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k_cache), gdim, gstr, box128,
-                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r1 = enc(&e.m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src.latent), gdim_l, gstr_l,
+                      box128, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    CUresult r2 = enc(&e.m64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(k_cache), gdim, gstr, box64,
+    CUresult r2 = enc(&e.m64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src.rope), gdim_r, gstr_r, box64,
                       es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
         e.valid = false;
-        return fail(MLA_ERR_ARG, "k_cache tensor map rejected by the driver (codes %d, %d): check alignment/strides",
+        return fail(MLA_ERR_ARG, "cache tensor map rejected by the driver (codes %d, %d): check alignment/strides",
                     (int)r1, (int)r2);
     }
-    e.ptr = k_cache; e.device = dev; e.num_blocks = sh->num_blocks; e.h_k = sh->h_k;
-    e.s0 = sh->k_stride[0]; e.s1 = sh->k_stride[1]; e.s2 = sh->k_stride[2];
+    e.src = src;
+    e.device = dev;
+    e.num_blocks = sh->num_blocks;
+    e.h_k = sh->h_k;
     e.valid = true;
     g_map_next = (g_map_next + 1) % kMapCache;
     *m128 = e.m128;
@@ -312,6 +345,10 @@ int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int
     memset(&p, 0, sizeof p);
     p.q = static_cast<const uint16_t *>(q);
     p.q_s0 = sh->q_stride[0]; p.q_s1 = sh->q_stride[1]; p.q_s2 = sh->q_stride[2];
+    p.q_rope = q ? p.q + MLA_HEAD_DIM_V : nullptr;   // concatenated q; the split call overrides it
+    p.qr_s0 = p.q_s0; p.qr_s1 = p.q_s1; p.qr_s2 = p.q_s2;
+    p.q_concat = 1;
+    p.rope_x0 = MLA_HEAD_DIM_V;                      // concatenated cache; the split call sets 0
     p.block_table = block_table;
     p.bt_stride = sh->bt_stride;
     p.seqlens = cache_seqlens;
@@ -337,9 +374,9 @@ int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int
     return MLA_OK;
 }
 
-int launch_splitkv(const mla_shape_t *sh, const void *k_cache, const Prepared &pr, cudaStream_t stream) {
+int launch_splitkv(const mla_shape_t *sh, const KvSource &src, const Prepared &pr, cudaStream_t stream) {
     CUtensorMap m128, m64;
-    int st = kcache_maps(sh, k_cache, &m128, &m64);
+    int st = kcache_maps(sh, src, &m128, &m64);
     if (st != MLA_OK) return st;
     mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
     cudaError_t e = cudaGetLastError();
@@ -556,7 +593,7 @@ int mla_decode_splitkv(const mla_shape_t *shape, const void *q, const void *k_ca
                      ws_bytes, true, &pr, &ds);
     if (st != MLA_OK) return st;
     if (shape->batch == 0) return MLA_OK;
-    return launch_splitkv(shape, k_cache, pr, reinterpret_cast<cudaStream_t>(stream));
+    return launch_splitkv(shape, concat_source(shape, k_cache), pr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
@@ -591,8 +628,53 @@ int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
     if (st != MLA_OK) return st;
     if (shape->batch == 0) return MLA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = launch_splitkv(shape, k_cache, pr, s);
+    st = launch_splitkv(shape, concat_source(shape, k_cache), pr, s);
     if (st != MLA_OK) return st;
+    return launch_combine(shape, pr, s);
+}
+
+int mla_decode_fwd_split(const mla_shape_t *shape, const mla_rope_strides_t *rope, const void *q_nope,
+                         const void *q_rope, const void *ctkv, const void *krope, const int32_t *block_table,
+                         const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float scale,
+                         int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    if (!rope) return fail(MLA_ERR_ARG, "rope strides are NULL");
+    int st = check_args(shape, q_nope, ctkv, block_table, cache_seqlens, md, num_splits, out, lse, true);
+    if (st != MLA_OK) return st;
+    if (!q_rope || !krope) return fail(MLA_ERR_ARG, "NULL tensor pointer");
+    if (!aligned16(q_rope) || !aligned16(krope)) return fail(MLA_ERR_ARG, "q_rope and krope must be 16-byte aligned");
+    for (int i = 0; i < 3; ++i) {
+        if (rope->q_rope_stride[i] <= 0 || rope->q_rope_stride[i] % 8 || rope->krope_stride[i] <= 0 ||
+            rope->krope_stride[i] % 8)
+            return fail(MLA_ERR_ARG, "rope strides must be positive multiples of 8 elements");
+    }
+    if (shape->q_stride[2] < MLA_HEAD_DIM_V || shape->k_stride[2] < MLA_HEAD_DIM_V ||
+        rope->q_rope_stride[2] < MLA_HEAD_DIM - MLA_HEAD_DIM_V || rope->krope_stride[2] < MLA_HEAD_DIM - MLA_HEAD_DIM_V)
+        return fail(MLA_ERR_ARG, "head strides smaller than the head's dims");
+    if (!ws && ws_bytes == 0) {
+        if ((st = internal_workspace(shape, reinterpret_cast<cudaStream_t>(stream), &ws, &ws_bytes)) != MLA_OK) return st;
+    }
+    Prepared pr;
+    DeviceState *ds = nullptr;
+    if ((st = prepare(shape, q_nope, ctkv, block_table, cache_seqlens, md, num_splits, scale, causal, out, lse, ws,
+                      ws_bytes, true, &pr, &ds)) != MLA_OK)
+        return st;
+    pr.p.q_rope = static_cast<const uint16_t *>(q_rope);
+    pr.p.qr_s0 = rope->q_rope_stride[0]; pr.p.qr_s1 = rope->q_rope_stride[1]; pr.p.qr_s2 = rope->q_rope_stride[2];
+    pr.p.rope_x0 = 0;
+    pr.p.q_concat = pr.p.q_rope == pr.p.q + MLA_HEAD_DIM_V && pr.p.qr_s0 == pr.p.q_s0 && pr.p.qr_s1 == pr.p.q_s1 &&
+                    pr.p.qr_s2 == pr.p.q_s2;
+    if (shape->batch == 0) return MLA_OK;
+    KvSource src;
+    src.latent = ctkv;
+    src.rope = krope;
+    for (int i = 0; i < 3; ++i) {
+        src.lat_stride[i] = shape->k_stride[i];
+        src.rope_stride[i] = rope->krope_stride[i];
+    }
+    src.lat_dims = MLA_HEAD_DIM_V;
+    src.rope_dims = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_splitkv(shape, src, pr, s)) != MLA_OK) return st;
     return launch_combine(shape, pr, s);
 }
 
@@ -649,7 +731,7 @@ int mla_decode_fwd_host(const mla_shape_t *shape, const void *q_host, const void
     if ((e = cudaMemcpyAsync(q_d, q_host, lay.size[kStQ], cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return cuda_fail(e, "copy of q");
     if ((e = cudaStreamWaitEvent(s, h->join, 0)) != cudaSuccess) return cuda_fail(e, "join of the schedule stream");
-    if ((st = launch_splitkv(&sh, k_cache, pr, s)) != MLA_OK) return st;
+    if ((st = launch_splitkv(&sh, concat_source(&sh, k_cache), pr, s)) != MLA_OK) return st;
     if ((st = launch_combine(&sh, pr, s)) != MLA_OK) return st;
     if (!out_direct && (e = cudaMemcpyAsync(out_host, out_d, lay.size[kStOut], cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "copy of out");

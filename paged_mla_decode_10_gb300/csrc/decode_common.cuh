@@ -17,8 +17,10 @@ constexpr int kErrTimeout = 1;
 constexpr int kErrBadBlock = 2;
 
 struct DecodeParams {
-    const uint16_t *q;             // bf16 (B, s_q, h_q, 576)
+    const uint16_t *q;             // bf16 latent dims of q: (B, s_q, h_q, >= 512)
     int64_t q_s0, q_s1, q_s2;
+    const uint16_t *q_rope;        // bf16 RoPE dims of q: (B, s_q, h_q, 64); q + 512 when q holds all 576
+    int64_t qr_s0, qr_s1, qr_s2;
     const int32_t *block_table;
     int64_t bt_stride;
     const int32_t *seqlens;
@@ -33,6 +35,8 @@ struct DecodeParams {
     int batch, s_q, h_q, h_k, hpk, rows;   // rows = R = s_q * h_q / h_k
     int num_blocks, max_blocks, num_parts, max_slots;
     int causal;
+    int q_concat;                  // q_rope == q + 512 with q's strides: one 576-dim row per query
+    int rope_x0;                   // first RoPE dim in the RoPE tensor map (512 over a 576-dim cache, else 0)
     float scale_log2;              // softmax_scale * log2(e)
 };
 

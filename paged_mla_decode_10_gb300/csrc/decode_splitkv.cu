@@ -119,11 +119,13 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
                         const uint32_t full = bar_addr(c, B_KFULL + st);
                         const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
                         mbar_arrive_expect_tx(full, kHalfBytes);
-                        // tensor map dims: {576 dims, h_k heads, 64 rows, num_blocks}
+                        // tensor maps: {latent dims, h_k heads, 64 rows, num_blocks} and
+                        // {RoPE dims, h_k heads, 64 rows, num_blocks} (576 dims from 512 on a
+                        // concatenated cache, 64 on a separate one)
 #pragma unroll
                         for (int a = 0; a < 4; ++a)
                             tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
-                        tma_load_4d(dst + 32768u, km64, full, 512 + 32 * cta, hk, 0, phys, policy);
+                        tma_load_4d(dst + 32768u, km64, full, p.rope_x0 + 32 * cta, hk, 0, phys, policy);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -246,6 +248,9 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
     const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
     const uint4 *qrow = reinterpret_cast<const uint4 *>(
         p.q + (int64_t)sg.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
+    const uint4 *rrow = p.q_concat ? qrow + 64
+                                   : reinterpret_cast<const uint4 *>(p.q_rope + (int64_t)sg.b * p.qr_s0 +
+                                                                     (int64_t)qi * p.qr_s1 + (int64_t)qh * p.qr_s2);
     uint32_t w0[64], w1[64];
     uint4 rope[4];
 #pragma unroll
@@ -256,7 +261,7 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
         w1[4 * v] = y.x; w1[4 * v + 1] = y.y; w1[4 * v + 2] = y.z; w1[4 * v + 3] = y.w;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) rope[k] = row_real ? __ldg(qrow + 64 + cta * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < 4; ++k) rope[k] = row_real ? __ldg(rrow + cta * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
     tmem_st_32x32b_x64(tmem_q, w0);
     tmem_st_32x32b_x64(tmem_q + 64u, w1);
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));

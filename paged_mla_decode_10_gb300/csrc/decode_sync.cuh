@@ -63,7 +63,7 @@ static __device__ __forceinline__ int checked_phys(const DecodeParams &p, int b,
 }
 
 // Asks L2 for the query rows [64 half, 64 half + 64) of row block rb of KV head
-// hk of sequence b (whole 576-dim rows), so that the softmax warps' loads of
+// hk of sequence b (their 512 latent and 64 RoPE dims), so that the loads of
 // the next segment's Q hit L2.  Warp-wide; rows that are not 16-byte aligned
 // are skipped.
 static __device__ __forceinline__ void prefetch_q_rows(const DecodeParams &p, int b, int rb, int hk, int half,
@@ -73,7 +73,14 @@ static __device__ __forceinline__ void prefetch_q_rows(const DecodeParams &p, in
         if (row_g >= p.rows) break;
         const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
         const uint16_t *row = p.q + (int64_t)b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2;
-        if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) bulk_prefetch_l2(row, kDqk * 2);
+        if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0) continue;
+        if (p.q_concat) {
+            bulk_prefetch_l2(row, kDqk * 2);   // one request per whole row
+        } else {
+            bulk_prefetch_l2(row, kDv * 2);
+            const uint16_t *rope = p.q_rope + (int64_t)b * p.qr_s0 + (int64_t)qi * p.qr_s1 + (int64_t)qh * p.qr_s2;
+            if ((reinterpret_cast<uintptr_t>(rope) & 15u) == 0) bulk_prefetch_l2(rope, (kDqk - kDv) * 2);
+        }
     }
 }
 

@@ -101,3 +101,25 @@ def test_host_decode_rejects_bad_arguments_before_any_cuda_call(lib):
     assert b"contiguous" in lib.mla_last_error()
     assert lib.mla_decode_fwd_host(*args(_shape(num_sm_parts=1025))) == 2                 # schedule limit
     assert lib.mla_decode_fwd_host(*args(_shape(head_dim=512))) == 1                      # bad shape
+
+
+def test_split_decode_rejects_bad_arguments_before_any_cuda_call(lib):
+    from paged_mla_decode_10_gb300._lib import MlaRopeStrides
+    dummy = ctypes.c_void_p(256)
+    sh = _shape(q_stride=(16 * 512, 16 * 512, 512), k_stride=(64 * 512, 512, 512))
+    rs = MlaRopeStrides()
+    for i, (a, b) in enumerate(zip((16 * 64, 16 * 64, 64), (64 * 64, 64, 64))):
+        rs.q_rope_stride[i], rs.krope_stride[i] = a, b
+
+    def call(rope=ctypes.byref(rs), q_rope=dummy, krope=dummy, shape=sh):
+        return lib.mla_decode_fwd_split(ctypes.byref(shape), rope, dummy, q_rope, dummy, krope, dummy, dummy, dummy,
+                                        dummy, ctypes.c_float(0.0), 0, dummy, dummy, dummy, 1 << 30, None)
+    assert call(rope=None) == 1                              # no rope strides
+    assert call(q_rope=None) == 1                            # NULL q_rope
+    assert call(krope=ctypes.c_void_p(264)) == 1             # krope not 16-byte aligned
+    rs.krope_stride[2] = 60
+    assert call() == 1                                       # stride not a multiple of 8
+    rs.krope_stride[2] = 56
+    assert call() == 1                                       # head stride below 64 dims
+    rs.krope_stride[2] = 64
+    assert call(shape=_shape(q_stride=(16 * 512, 16 * 512, 504), k_stride=(64 * 512, 512, 512))) == 1
