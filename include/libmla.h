@@ -50,7 +50,7 @@ typedef struct CUstream_st *mla_stream_t; /* same handle as cudaStream_t */
 enum {
     MLA_OK = 0,
     MLA_ERR_ARG = 1,         /* invalid argument: shape, stride, alignment or NULL pointer   */
-    MLA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (see each call)  */
+    MLA_ERR_UNSUPPORTED = 2, /* valid request outside what libmla implements (see each call) */
     MLA_ERR_ARCH = 3,        /* current device is not compute capability 10.3 (sm_103)       */
     MLA_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed                          */
     MLA_ERR_WORKSPACE = 5,   /* workspace pointer NULL or smaller than mla_workspace_size     */
