@@ -251,19 +251,38 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
     const uint4 *rrow = p.q_concat ? qrow + 64
                                    : reinterpret_cast<const uint4 *>(p.q_rope + (int64_t)sg.b * p.qr_s0 +
                                                                      (int64_t)qi * p.qr_s1 + (int64_t)qh * p.qr_s2);
-    uint32_t w0[64], w1[64];
+    // 32-byte loads (one L2 sector each) where the rows allow, else pairs of 16-byte ones;
+    // two rounds of 128 + 32 bytes (the first with the RoPE dims), each stored to TMEM
+    const bool wide = ((reinterpret_cast<uintptr_t>(qrow) | reinterpret_cast<uintptr_t>(rrow)) & 31u) == 0;
+    auto load32 = [&](const uint4 *src, uint32_t *dst) {
+        if (!row_real) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = 0u;
+        } else if (wide) {
+            ldg_nc_v8(src, dst);
+        } else {
+            const uint4 a = __ldg(src), b = __ldg(src + 1);
+            dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+            dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
+        }
+    };
     uint4 rope[4];
+    {
+        uint32_t w[64], t[16];
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
-        const uint4 x = row_real ? __ldg(qrow + cta * 32 + v) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 y = row_real ? __ldg(qrow + cta * 32 + 16 + v) : make_uint4(0u, 0u, 0u, 0u);
-        w0[4 * v] = x.x; w0[4 * v + 1] = x.y; w0[4 * v + 2] = x.z; w0[4 * v + 3] = x.w;
-        w1[4 * v] = y.x; w1[4 * v + 1] = y.y; w1[4 * v + 2] = y.z; w1[4 * v + 3] = y.w;
+        for (int v = 0; v < 8; ++v) load32(qrow + cta * 32 + 2 * v, &w[8 * v]);
+        load32(rrow + cta * 4, &t[0]);
+        load32(rrow + cta * 4 + 2, &t[8]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rope[k] = make_uint4(t[4 * k], t[4 * k + 1], t[4 * k + 2], t[4 * k + 3]);
+        tmem_st_32x32b_x64(tmem_q, w);
     }
+    {
+        uint32_t w[64];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) rope[k] = row_real ? __ldg(rrow + cta * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-    tmem_st_32x32b_x64(tmem_q, w0);
-    tmem_st_32x32b_x64(tmem_q + 64u, w1);
+        for (int v = 0; v < 8; ++v) load32(qrow + cta * 32 + 16 + 2 * v, &w[8 * v]);
+        tmem_st_32x32b_x64(tmem_q + 64u, w);
+    }
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 #pragma unroll
     for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz64_offset(r, k)) = rope[k];

@@ -252,6 +252,12 @@ __host__ __device__ constexpr uint32_t swz64_offset(uint32_t row, uint32_t chunk
 // ----------------------------------------------------------------------------
 // misc math
 // ----------------------------------------------------------------------------
+// 32-byte read-only global load (one L2 sector); p must be 32-byte aligned.
+__device__ __forceinline__ void ldg_nc_v8(const void *p, uint32_t *r) {
+    asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "l"(p));
+}
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
