@@ -68,9 +68,18 @@ __global__ void __launch_bounds__(kThreadsCombine, 4) mla_combine_kernel(const _
         for (int sp = 0; sp < kChunk; ++sp) {
             const bool in = s0 + sp < n;
             ls[sp] = in ? __ldg(p.ws_lse + prow0 + (s0 + sp) * stride) * kLog2e : -INFINITY;
+            // the lane's 64 bytes of the partial row as two 32-byte (one-sector) loads
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = 0u;
+            if (in) {
+                ldg_nc_v8(src + (s0 + sp) * sstride, &w[0]);
+                ldg_nc_v8(src + (s0 + sp) * sstride + 2, &w[8]);
+            }
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-                x[sp][v] = in ? __ldg(src + (s0 + sp) * sstride + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[sp][v] = make_float4(__uint_as_float(w[4 * v]), __uint_as_float(w[4 * v + 1]),
+                                       __uint_as_float(w[4 * v + 2]), __uint_as_float(w[4 * v + 3]));
         }
         float mc = m;
 #pragma unroll
