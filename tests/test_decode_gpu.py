@@ -47,6 +47,19 @@ def test_small_cases_multi_tile(case, parts):
     assert_close(out, lse, ref_o, ref_l, where=f"{name} parts={parts}")
 
 
+@pytest.mark.parametrize("case", [
+    ("rows_1024_causal", 8, 128, [70, 300, 9], 1, True),    # R = 1024, the limit: eight 128-row blocks
+    ("rows_40", 1, 40, [129, 64, 1000], 1, False),          # R = 40: a partly filled second warp
+    ("hk4_rows_32", 2, 64, [65, 500], 4, True),             # four KV heads of 32 rows (s_q 2 x 16 heads)
+])
+def test_row_count_edges(case):
+    name, s_q, h_q, Ls, h_k, causal = case
+    inp = _custom(name, len(Ls), s_q, h_q, Ls, h_k=h_k, causal=causal, seed=len(Ls) * 7 + h_q)
+    out, lse, md, ns = run_gpu(inp)
+    ref_o, ref_l = oracle(inp)
+    assert_close(out, lse, ref_o, ref_l, where=name)
+
+
 def test_empty_and_invisible_rows():
     # L = 0 sequence; causal L=1 with s_q=3 (rows i=0,1 see nothing)
     inp = _custom("edge", 3, 3, 16, [0, 1, 130], causal=True, seed=4)
