@@ -5,7 +5,11 @@
 // stacked as the tcgen05 M dimension) against the part's 64-row pages of the
 // latent cache (FlashMLA-PyTorch page, flash_mla_interface.py,
 // flash_mla_with_kvcache docstring: q (B, s_q, h_q, 576), k_cache
-// (num_blocks, 64, h_k, 576), V = the first 512 dims of the cache rows).
+// (num_blocks, 64, h_k, 576), V = the first 512 dims of the cache rows).  The
+// 64 RoPE dims of q and of the cache may instead live in tensors of their own
+// (the Ascend ATB MLA page's qRope / kRope): the RoPE query dims are read
+// through DecodeParams::q_rope and the RoPE cache dims through the second
+// tensor map, whose boxes start at DecodeParams::rope_x0.
 //
 // Work split.  One part is processed by a cluster of two CTAs on two SMs.
 // CTA c owns the V dims [256c, 256c + 256) and, for the QK^T contraction,
