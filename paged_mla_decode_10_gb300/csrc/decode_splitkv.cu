@@ -316,7 +316,9 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
-    uint8_t *row = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT + (uint32_t)r * 256u;
+    // staging layout of a warp's 8 KB: [column half][32 rows][128 B], 16-byte chunks swizzled by row
+    uint8_t *half0 = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT +
+                     (uint32_t)q * 8192u + (uint32_t)lane * 128u;
 
     const uint32_t tmem_q = tmem + lane_base + TM_Q;
 
@@ -345,17 +347,25 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
             if (!ok) break;
+            // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch)
-                *reinterpret_cast<uint4 *>(row + ((ch ^ (r & 7)) << 4)) =
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(half0 + ((ch ^ (lane & 7)) << 4)) =
                     make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
             if (!ok) break;
-            if (lane == 0)
-                bulk_copy_to_peer(xin_peer + b * kXBytes, c.base + OFF_XOUT + (uint32_t)q * 8192u, 8192u,
-                                  b ? xfull_peer[1] : xfull_peer[0]);
+            const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
+            const uint32_t src = c.base + OFF_XOUT + (uint32_t)q * 8192u, dst = xin_peer + b * kXBytes;
+            if (lane == 0) bulk_copy_to_peer(dst, src, 4096u, xfull);
+#pragma unroll
+            for (int ch = 8; ch < 16; ++ch)
+                *reinterpret_cast<uint4 *>(half0 + 4096 + (((ch - 8) ^ (lane & 7)) << 4)) =
+                    make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) bulk_copy_to_peer(dst + 4096u, src + 4096u, 4096u, xfull);
         }
         if (!ok) break;
         // Q of the next segment, once every MMA of this one has completed; the
@@ -391,7 +401,9 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const uint32_t peer = (uint32_t)(cta ^ 1);
 
     // shared addresses
-    const uint32_t xrow_local[2] = {c.base + OFF_XIN + r * 256u, c.base + OFF_XIN + kXBytes + r * 256u};
+    // this row in the landing slots: warp block of 8 KB = [column half][32 rows][128 B]
+    const uint32_t xrow_local[2] = {c.base + OFF_XIN + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 128u,
+                                    c.base + OFF_XIN + kXBytes + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 128u};
     const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE), peer),
                                     mapa_shared(bar_addr(c, B_XINFREE + 1), peer)};
     const uint32_t stagefree_peer = mapa_shared(bar_addr(c, B_STAGEFREE), peer);
@@ -440,7 +452,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
-                    smem_gen + ((sb ? xrow_local[1] : xrow_local[0]) - c.base) + ((ch ^ (r & 7)) << 4));
+                    smem_gen + ((sb ? xrow_local[1] : xrow_local[0]) - c.base) + (ch >> 3) * 4096 +
+                    (((ch & 7) ^ (r & 7)) << 4));
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
             __syncwarp();
