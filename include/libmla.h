@@ -266,6 +266,34 @@ int mla_decode_fwd_split(const mla_shape_t *shape, const mla_rope_strides_t *rop
                          void *workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * mla_decode_fwd over an e4m3 (FP8, 1 sign, 4 exponent, 3 mantissa bits)
+ * query and latent cache, with the two fused product scales of the FlashInfer
+ * page (trtllm_batch_decode_with_kv_cache_mla, the note on bmm1_scale and
+ * bmm2_scale):
+ *   s_t = bmm1_scale * sum_{d < 576} q[d] * k[t][d]
+ *   out = bmm2_scale * sum_t softmax(s)_t * k[t][0:512]      (bf16)
+ *   softmax_lse = ln sum_t exp(s_t)                           (fp32)
+ * with q and k the e4m3 values as stored.  bmm1_scale folds the query and key
+ * dequantisation scales into the softmax scale; bmm2_scale is the value
+ * dequantisation scale.
+ *   q        (batch, s_q, h_q, 576) e4m3 bytes      strides shape->q_stride (elements = bytes)
+ *   k_cache  (num_blocks, 64, h_k, 576) e4m3 bytes  strides shape->k_stride
+ *   out      (batch, s_q, h_q, 512) bf16, softmax_lse (batch, h_q, s_q) fp32, as mla_decode_fwd
+ * Masking, schedule (mla_get_metadata), workspace (NULL = internal) and the
+ * two launches are those of mla_decode_fwd.  The probabilities are rounded to
+ * e4m3 for the PV product (the denominator sums them unrounded), so the output
+ * differs from the exact value by up to 2^-4 of each probability times its
+ * value row.  Errors: as mla_decode_fwd, and MLA_ERR_ARG when bmm1_scale is
+ * not positive and finite, bmm2_scale not finite, or a q / k_cache stride is
+ * not a multiple of 16 bytes.
+ */
+int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_cache,
+                       const int32_t *block_table, const int32_t *cache_seqlens,
+                       const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                       float bmm1_scale, float bmm2_scale, int causal, void *out, float *softmax_lse,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * One whole decode step from host buffers: copies q, block_table and
  * cache_seqlens to the device, computes the schedule (mla_get_metadata with
  * shape->num_sm_parts parts), decodes (mla_decode_fwd) and returns out and

@@ -196,6 +196,40 @@ def mla_decode_fwd_split(q_nope, q_rope, ctkv, krope, block_table, cache_seqlens
     return out, softmax_lse
 
 
+_E4M3 = tuple(t for t in (getattr(torch, "float8_e4m3fn", None), torch.uint8) if t is not None)
+
+
+def mla_decode_fwd_fp8(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_scheduler_metadata, num_splits,
+                       bmm1_scale, bmm2_scale=1.0, causal=False, out=None, softmax_lse=None, workspace=None,
+                       stream=None):
+    """mla_decode_fwd over an e4m3 query (B, s_q, h_q, 576) and latent cache (num_blocks, 64, h_k, 576),
+    given as float8_e4m3fn or uint8 (the e4m3 bytes) CUDA tensors, with the fused product scales:
+    logits = bmm1_scale * q.k, out = bmm2_scale * softmax(logits) V.  Returns (out bf16, softmax_lse fp32)."""
+    L = _lib.load()
+    _require(q.dim() == 4 and k_cache.dim() == 4, "q and k_cache must be 4-D")
+    _require(q.dtype in _E4M3 and k_cache.dtype in _E4M3 and q.is_cuda and k_cache.is_cuda,
+             "q and k_cache must be float8_e4m3fn or uint8 CUDA tensors")
+    _require(block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32,
+             "block_table and cache_seqlens must be int32")
+    B, s_q, h_q, _ = q.shape
+    if out is None:
+        out = torch.empty((B, s_q, h_q, head_dim_v), dtype=torch.bfloat16, device=q.device)
+    if softmax_lse is None:
+        softmax_lse = torch.empty((B, h_q, s_q), dtype=torch.float32, device=q.device)
+    _require(out.dtype == torch.bfloat16, "out must be bf16")
+    _require(softmax_lse.is_contiguous() and softmax_lse.dtype == torch.float32, "softmax_lse: contiguous fp32")
+    cache_seqlens = cache_seqlens.contiguous()
+    sh = make_shape(q, k_cache, block_table, out.stride()[:3], tile_scheduler_metadata.shape[0], head_dim_v)
+    need = mla_workspace_size(sh)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    check(L.mla_decode_fwd_fp8(ctypes.byref(sh), _ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(cache_seqlens),
+                               _ptr(tile_scheduler_metadata), _ptr(num_splits), float(bmm1_scale), float(bmm2_scale),
+                               int(bool(causal)), _ptr(out), _ptr(softmax_lse), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "mla_decode_fwd_fp8")
+    return out, softmax_lse
+
+
 def mla_decode_fwd_host(q, k_cache, block_table, cache_seqlens, head_dim_v, softmax_scale=None, causal=False,
                         num_sm_parts=None, out=None, softmax_lse=None, stream=None):
     """One decode step from host tensors: q, block_table, cache_seqlens and the results live in host

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla.so")
-SOURCES = ["api.cu", "decode_splitkv.cu", "combine.cu", "metadata.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode_splitkv.cu", "decode_splitkv_fp8.cu", "combine.cu", "metadata.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

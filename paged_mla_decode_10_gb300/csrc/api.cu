@@ -16,10 +16,13 @@
 namespace mla {
 __global__ void mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
                                    const __grid_constant__ DecodeParams p);
+__global__ void mla_splitkv_kernel_f8(const __grid_constant__ CUtensorMap km128,
+                                      const __grid_constant__ CUtensorMap km64, const __grid_constant__ DecodeParams p);
 __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
 __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
 size_t metadata_smem_bytes(int batch, int parts);
 uint32_t splitkv_smem_bytes();
+uint32_t splitkv_f8_smem_bytes();
 uint32_t splitkv_threads();
 uint32_t combine_threads();
 uint32_t combine_rows_per_block();
@@ -87,6 +90,9 @@ int device_state(DeviceState **out) {
             if ((e = cudaFuncSetAttribute(mla_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
                 cudaSuccess)
                 return cuda_fail(e, "cudaFuncSetAttribute(splitkv)");
+            if ((e = cudaFuncSetAttribute(mla_splitkv_kernel_f8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)splitkv_f8_smem_bytes())) != cudaSuccess)
+                return cuda_fail(e, "cudaFuncSetAttribute(splitkv e4m3)");
             if ((e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)metadata_smem_bytes(kMaxBatchMetadata, kMaxPartsMetadata))) != cudaSuccess)
                 return cuda_fail(e, "cudaFuncSetAttribute(metadata)");
@@ -122,10 +128,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Where the cache rows come from: the latent dims (TMA boxes of 64 dims) and
-// the RoPE dims (a box of 32), either one tensor of 576-dim rows or two
-// tensors (512 and 64 dims).  Strides in elements: {block, row, kv-head}.
+// Where the cache rows come from: the latent dims (TMA boxes of 128-byte rows:
+// 64 bf16 or 128 e4m3 dims) and the RoPE dims (a box of 32), either one
+// tensor of 576-dim rows or two tensors (512 and 64 dims).  Strides in
+// elements: {block, row, kv-head}.
 struct KvSource {
+    int elem = 2;              // bytes per element: 2 (bf16) or 1 (e4m3)
     const void *latent;
     int64_t lat_stride[3];
     int lat_dims;              // extent of the latent tensor's last dimension (576 or 512)
@@ -169,7 +177,7 @@ int get_encoder(EncodeTiledFn *fn) {
 }
 
 bool same_source(const KvSource &a, const KvSource &b) {
-    return a.latent == b.latent && a.rope == b.rope && a.lat_dims == b.lat_dims && a.rope_dims == b.rope_dims &&
+    return a.elem == b.elem && a.latent == b.latent && a.rope == b.rope && a.lat_dims == b.lat_dims && a.rope_dims == b.rope_dims &&
            !memcmp(a.lat_stride, b.lat_stride, sizeof a.lat_stride) &&
            !memcmp(a.rope_stride, b.rope_stride, sizeof a.rope_stride);
 }
@@ -194,18 +202,24 @@ int kcache_maps(const mla_shape_t *sh, const KvSource &src, CUtensorMap *m128, C
                                   (cuuint64_t)sh->num_blocks};
     const cuuint64_t gdim_r[4] = {(cuuint64_t)src.rope_dims, (cuuint64_t)sh->h_k, (cuuint64_t)sh->page_block_size,
                                   (cuuint64_t)sh->num_blocks};
-    const cuuint64_t gstr_l[3] = {(cuuint64_t)src.lat_stride[2] * 2, (cuuint64_t)src.lat_stride[1] * 2,
-                                  (cuuint64_t)src.lat_stride[0] * 2};
-    const cuuint64_t gstr_r[3] = {(cuuint64_t)src.rope_stride[2] * 2, (cuuint64_t)src.rope_stride[1] * 2,
-                                  (cuuint64_t)src.rope_stride[0] * 2};
-    const cuuint32_t box128[4] = {64, 1, 64, 1}, box64[4] = {32, 1, 64, 1}, es[4] = {1, 1, 1, 1};
+    const cuuint64_t eb = (cuuint64_t)src.elem;
+    const cuuint64_t gstr_l[3] = {(cuuint64_t)src.lat_stride[2] * eb, (cuuint64_t)src.lat_stride[1] * eb,
+                                  (cuuint64_t)src.lat_stride[0] * eb};
+    const cuuint64_t gstr_r[3] = {(cuuint64_t)src.rope_stride[2] * eb, (cuuint64_t)src.rope_stride[1] * eb,
+                                  (cuuint64_t)src.rope_stride[0] * eb};
+    // latent boxes of 128-byte rows (SW128); RoPE boxes of 32 dims: 64-byte rows (SW64) in bf16,
+    // 32-byte rows (SW32) in e4m3
+    const cuuint32_t box128[4] = {(cuuint32_t)(128 / src.elem), 1, 64, 1}, box64[4] = {32, 1, 64, 1},
+                     es[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = src.elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle rsw = src.elem == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
     MapEntry &e = g_maps[g_map_next];
-    CUresult r1 = enc(&e.m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src.latent), gdim_l, gstr_l,
-                      box128, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    CUresult r2 = enc(&e.m64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src.rope), gdim_r, gstr_r, box64,
-                      es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r1 = enc(&e.m128, dt, 4, const_cast<void *>(src.latent), gdim_l, gstr_l, box128, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r2 = enc(&e.m64, dt, 4, const_cast<void *>(src.rope), gdim_r, gstr_r, box64, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, rsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) {
         e.valid = false;
         return fail(MLA_ERR_ARG, "cache tensor map rejected by the driver (codes %d, %d): check alignment/strides",
@@ -378,7 +392,10 @@ int launch_splitkv(const mla_shape_t *sh, const KvSource &src, const Prepared &p
     CUtensorMap m128, m64;
     int st = kcache_maps(sh, src, &m128, &m64);
     if (st != MLA_OK) return st;
-    mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
+    if (src.elem == 1)
+        mla_splitkv_kernel_f8<<<pr.grid, splitkv_threads(), splitkv_f8_smem_bytes(), stream>>>(m128, m64, pr.p);
+    else
+        mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
     return MLA_OK;
@@ -630,6 +647,38 @@ int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     st = launch_splitkv(shape, concat_source(shape, k_cache), pr, s);
     if (st != MLA_OK) return st;
+    return launch_combine(shape, pr, s);
+}
+
+int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+                       const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float bmm1_scale,
+                       float bmm2_scale, int causal, void *out, float *lse, void *ws, size_t ws_bytes,
+                       mla_stream_t stream) {
+    int st = check_args(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, true);
+    if (st != MLA_OK) return st;
+    if (!(bmm1_scale > 0.f) || !std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale))
+        return fail(MLA_ERR_ARG, "bmm1_scale must be positive and finite, bmm2_scale finite");
+    for (int i = 0; i < 3; ++i)
+        if (shape->q_stride[i] % 16 || shape->k_stride[i] % 16)
+            return fail(MLA_ERR_ARG, "e4m3 q and k_cache strides must be multiples of 16 elements");
+    if (!ws && ws_bytes == 0) {
+        st = internal_workspace(shape, reinterpret_cast<cudaStream_t>(stream), &ws, &ws_bytes);
+        if (st != MLA_OK) return st;
+    }
+    Prepared pr;
+    DeviceState *ds = nullptr;
+    st = prepare(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, bmm1_scale, causal, out, lse, ws,
+                 ws_bytes, true, &pr, &ds);
+    if (st != MLA_OK) return st;
+    pr.p.q = nullptr;
+    pr.p.q_rope = nullptr;
+    pr.p.q8 = static_cast<const uint8_t *>(q);
+    pr.p.out_scale = bmm2_scale;
+    if (shape->batch == 0) return MLA_OK;
+    KvSource src = concat_source(shape, k_cache);
+    src.elem = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = launch_splitkv(shape, src, pr, s)) != MLA_OK) return st;
     return launch_combine(shape, pr, s);
 }
 

@@ -37,7 +37,9 @@ struct DecodeParams {
     int causal;
     int q_concat;                  // q_rope == q + 512 with q's strides: one 576-dim row per query
     int rope_x0;                   // first RoPE dim in the RoPE tensor map (512 over a 576-dim cache, else 0)
-    float scale_log2;              // softmax_scale * log2(e)
+    float scale_log2;              // softmax_scale * log2(e) (bmm1_scale * log2(e) for e4m3 inputs)
+    const uint8_t *q8;             // e4m3 q (B, s_q, h_q, 576), strides q_s0..2 in bytes (e4m3 kernel only)
+    float out_scale;               // bmm2_scale: factor on the output of the e4m3 kernel
 };
 
 // One contiguous run of blocks of one sequence assigned to a part.

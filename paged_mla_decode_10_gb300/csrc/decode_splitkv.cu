@@ -34,6 +34,15 @@
 //   warp  8    TMA producer: page gather through block_table, Q prefetch
 //   warp  9    MMA issuer (one lane) + TMEM allocation
 //
+// e4m3 variant.  The same source compiled with MLA_F8=1 (decode_splitkv_fp8.cu)
+// gives mla_splitkv_kernel_f8 for an e4m3 query and cache with the two fused
+// product scales of the FlashInfer page (trtllm_batch_decode_with_kv_cache_mla,
+// bmm1_scale / bmm2_scale note): the MMAs are kind::f8f6f4 (K = 32), a page
+// half is 18,432 B (two 128-dim SW128 boxes and one 32-byte SW32 RoPE box),
+// the ring has six stages, Q fills TMEM columns [384,448) (e4m3 quads), P is
+// rounded to e4m3 (quads, 16 columns) for the PV MMA while the denominator
+// sums the fp32 values, and the epilogue multiplies by bmm2_scale.
+//
 // Online softmax (log2 domain) with lazy rescaling: the running max is only
 // raised when a page's max exceeds it by more than 8 (a factor of 256), so
 // the O correction (TMEM read-modify-write) is rare after the first pages.
@@ -54,11 +63,23 @@ namespace mla {
 
 namespace {
 
+#ifndef MLA_F8
+#define MLA_F8 0
+#endif
+#if MLA_F8
+constexpr int kStages = 6;
+constexpr int kLatBoxes = 2;                    // 128 e4m3 dims (128 B rows) per latent box
+constexpr uint32_t kRopeRow = 32;               // bytes per RoPE row: 32 e4m3 dims, SW32
+#else
 constexpr int kStages = 3;
-constexpr uint32_t kHalfBytes = 36864;          // one CTA's 288-dim half of a page
+constexpr int kLatBoxes = 4;                    // 64 bf16 dims (128 B rows) per latent box
+constexpr uint32_t kRopeRow = 64;               // bytes per RoPE row: 32 bf16 dims, SW64
+#endif
+constexpr uint32_t kRopeOff = kLatBoxes * 8192u;              // RoPE box within a stage
+constexpr uint32_t kHalfBytes = kRopeOff + 64u * kRopeRow;    // one CTA's 288-dim half of a page
 constexpr uint32_t kXBytes = 32768;             // one 128 x 64 fp32 partial-logit tile
-constexpr uint32_t OFF_QR = 0;                  // 128 rows x 64 B, SW64
-constexpr uint32_t OFF_K = 8192;
+constexpr uint32_t OFF_QR = 0;                  // Q RoPE half: 128 rows x kRopeRow
+constexpr uint32_t OFF_K = 128u * kRopeRow;
 constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (2 slots)
 constexpr uint32_t OFF_XOUT = OFF_XIN + 2 * kXBytes;          // our partial tile, staged for the DMA
 constexpr uint32_t OFF_EPI = OFF_XOUT + kXBytes;          // epilogue staging, one tile per softmax warp
@@ -127,9 +148,10 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
                         // {RoPE dims, h_k heads, 64 rows, num_blocks} (576 dims from 512 on a
                         // concatenated cache, 64 on a separate one)
 #pragma unroll
-                        for (int a = 0; a < 4; ++a)
-                            tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + 64 * a, hk, 0, phys, policy);
-                        tma_load_4d(dst + 32768u, km64, full, p.rope_x0 + 32 * cta, hk, 0, phys, policy);
+                        for (int a = 0; a < kLatBoxes; ++a)
+                            tma_load_4d(dst + a * 8192u, km128, full, 256 * cta + (256 / kLatBoxes) * a, hk, 0, phys,
+                                        policy);
+                        tma_load_4d(dst + kRopeOff, km64, full, p.rope_x0 + 32 * cta, hk, 0, phys, policy);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -155,6 +177,14 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
     if (!ok) return false;
     tc_fence_after();
     if (lane == 0) {
+#if MLA_F8
+        constexpr uint32_t idPV = make_idesc_e4m3(128, 256, false, true);
+        // V of this stage, MN-major: 2 boxes of 128 dims (LBO 8 KB), 8-key groups 1 KB apart
+        const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
+        const uint32_t pa = tmem + TM_S + 64u * pb;   // P (e4m3 quads, 8 columns per 32 keys) where its S was
+        umma_ts_f8(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
+        umma_ts_f8(tmem + TM_O, pa + 8u, bd0 + 256u, idPV, 1u);   // +32 keys = +4096 B
+#else
         constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
         // V of this stage, MN-major: 4 boxes of 64 dims (LBO 8 KB), 8-key groups 1 KB apart
         const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
@@ -163,6 +193,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
 #pragma unroll
         for (int kk = 1; kk < 4; ++kk)   // +16 keys = +2048 B = +128 in the descriptor's 16-byte units
             umma_ts(tmem + TM_O, pa + 8u * kk, bd0 + 128u * kk, idPV, 1u);
+#endif
         umma_commit(bar_addr(c, B_KEMPTY + st));
         umma_commit(bar_addr(c, B_PVDONE));
     }
@@ -176,7 +207,11 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
     Segment s;
     uint32_t it = 0, g = 0;
     bool ok = true;
+#if MLA_F8
+    constexpr uint32_t idS = make_idesc_e4m3(128, 64, false, false);
+#else
     constexpr uint32_t idS = make_idesc_bf16(128, 64, false, false);
+#endif
     while (ok && walk.next(p, s)) {
         ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_QREADY), g & 1u));
         if (!ok) break;
@@ -194,10 +229,11 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 // P.V product would turn 0 * NaN into NaN, so zero them here.
                 uint8_t *gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(stage));
                 const int rows = kPage - tail;
-                for (int idx = lane; idx < rows * 36; idx += 32) {
-                    const int r = tail + idx / 36, ch = idx % 36;
-                    uint8_t *dst = ch < 32 ? gen + (ch >> 3) * 8192 + r * 128 + (ch & 7) * 16
-                                           : gen + 32768 + r * 64 + (ch - 32) * 16;
+                constexpr int kLatCh = kLatBoxes * 8, kRowCh = kLatCh + (int)kRopeRow / 16;   // 16-byte chunks
+                for (int idx = lane; idx < rows * kRowCh; idx += 32) {
+                    const int r = tail + idx / kRowCh, ch = idx % kRowCh;
+                    uint8_t *dst = ch < kLatCh ? gen + (ch >> 3) * 8192 + r * 128 + (ch & 7) * 16
+                                               : gen + kRopeOff + r * kRopeRow + (ch - kLatCh) * 16;
                     *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -210,14 +246,25 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 const uint32_t dS = tmem + TM_S + 64u * sb;
                 // K-major page boxes: +32 B per 16-dim k-step, +8 KB per 64-dim box (16-byte units)
                 const uint64_t bk = make_sdesc(stage, 16, 1024, kSwizzle128B);
+#if MLA_F8
+                // 8 steps of 32 latent dims: 4 per 128-byte box row (+32 B), +8 KB per box
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts_f8(dS, tmem + TM_Q + 8u * kk, bk + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idS,
+                               kk > 0 ? 1u : 0u);
+                const uint64_t aq = make_sdesc(c.base + OFF_QR, 16, 256, kSwizzle32B);
+                const uint64_t br = make_sdesc(stage + kRopeOff, 16, 256, kSwizzle32B);
+                umma_ss_f8(dS, aq, br, idS, 1u);
+#else
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk)
                     umma_ts(dS, tmem + TM_Q + 8u * kk, bk + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idS,
                             kk > 0 ? 1u : 0u);
                 const uint64_t aq = make_sdesc(c.base + OFF_QR, 16, 512, kSwizzle64B);
-                const uint64_t br = make_sdesc(stage + 32768u, 16, 512, kSwizzle64B);
+                const uint64_t br = make_sdesc(stage + kRopeOff, 16, 512, kSwizzle64B);
                 umma_ss(dS, aq, br, idS, 1u);
                 umma_ss(dS, aq + 2u, br + 2u, idS, 1u);
+#endif
                 umma_commit(bar_addr(c, B_SFULL + sb));
             }
             __syncwarp();
@@ -250,11 +297,19 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
     const int row_g = rb * kRowsPerBlock + r;
     const bool row_real = row_g < p.rows;
     const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
+#if MLA_F8
+    // e4m3 row of 576 bytes: latent bytes [256 cta, +256) -> TMEM columns 0-63
+    // (quads), RoPE bytes [512 + 32 cta, +32) -> smem (SW32)
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(
+        p.q8 + (int64_t)sg.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
+    const uint4 *rrow = qrow + 32;
+#else
     const uint4 *qrow = reinterpret_cast<const uint4 *>(
         p.q + (int64_t)sg.b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2);
     const uint4 *rrow = p.q_concat ? qrow + 64
                                    : reinterpret_cast<const uint4 *>(p.q_rope + (int64_t)sg.b * p.qr_s0 +
                                                                      (int64_t)qi * p.qr_s1 + (int64_t)qh * p.qr_s2);
+#endif
     // 32-byte loads (one L2 sector each) where the rows allow, else pairs of 16-byte ones;
     // two rounds of 128 + 32 bytes (the first with the RoPE dims), each stored to TMEM
     const bool wide = ((reinterpret_cast<uintptr_t>(qrow) | reinterpret_cast<uintptr_t>(rrow)) & 31u) == 0;
@@ -270,6 +325,20 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
             dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
         }
     };
+#if MLA_F8
+    {
+        uint32_t w[64], t[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) load32(qrow + cta * 16 + 2 * v, &w[8 * v]);
+        load32(rrow + cta * 2, t);
+        tmem_st_32x32b_x64(tmem_q, w);
+        uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz32_offset(r, k)) =
+                make_uint4(t[4 * k], t[4 * k + 1], t[4 * k + 2], t[4 * k + 3]);
+    }
+#else
     uint4 rope[4];
     {
         uint32_t w[64], t[16];
@@ -290,6 +359,7 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 #pragma unroll
     for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(smem_gen + OFF_QR + swz64_offset(r, k)) = rope[k];
+#endif
     tmem_st_wait();
     fence_proxy_async_smem();
     tc_fence_before();
@@ -480,6 +550,19 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             }
             const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
             const float c2 = p.scale_log2;
+#if MLA_F8
+            uint32_t pk[16];
+            float psum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float p0 = ex2_approx(fmaf(sv[4 * j], c2, neg_m));
+                const float p1 = ex2_approx(fmaf(sv[4 * j + 1], c2, neg_m));
+                const float p2 = ex2_approx(fmaf(sv[4 * j + 2], c2, neg_m));
+                const float p3 = ex2_approx(fmaf(sv[4 * j + 3], c2, neg_m));
+                pk[j] = pack_e4m3x4(p0, p1, p2, p3);   // P <= 2^8 (lazy rescale), within e4m3's 448
+                psum += (p0 + p1) + (p2 + p3);         // fp32 terms: the denominator, and so lse, stays exact
+            }
+#else
             uint32_t pk[32];
             float psum = 0.f;
 #pragma unroll
@@ -489,13 +572,18 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 pk[j] = pack_bf16x2(p0, p1);
                 psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
             }
+#endif
             l_sum += psum;
             // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
             // once the exchange warps have copied that S out
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), ph));
             if (!ok) break;
             tc_fence_after();
+#if MLA_F8
+            tmem_st_32x32b_x16(tmem + lane_base + TM_S + 64u * sb, pk);
+#else
             tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, pk);
+#endif
             // ---- lazy O correction, after PV(it - 1) has landed in TMEM
             if (__any_sync(0xffffffffu, raise && o_live)) {
                 ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PVDONE), (it - 1) & 1u));
@@ -525,7 +613,11 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
         tc_fence_after();
         if (warp_active) {
             const bool live = l_sum > 0.f;
+#if MLA_F8
+            const float inv = live ? p.out_scale / l_sum : 0.f;
+#else
             const float inv = live ? 1.f / l_sum : 0.f;
+#endif
             float lse_nat = -INFINITY;
             if (live) {
                 float lg;
@@ -550,8 +642,16 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 
 }  // namespace
 
+#if MLA_F8
+#define MLA_SPLITKV_KERNEL mla_splitkv_kernel_f8
+#define MLA_SPLITKV_SMEM_BYTES splitkv_f8_smem_bytes
+#else
+#define MLA_SPLITKV_KERNEL mla_splitkv_kernel
+#define MLA_SPLITKV_SMEM_BYTES splitkv_smem_bytes
+#endif
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
+MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
                    const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -630,7 +730,9 @@ mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_const
     cluster_wait();
 }
 
-uint32_t splitkv_smem_bytes() { return kSmemBytes; }
+uint32_t MLA_SPLITKV_SMEM_BYTES() { return kSmemBytes; }
+#if !MLA_F8
 uint32_t splitkv_threads() { return kThreads; }
+#endif
 
 }  // namespace mla

@@ -72,6 +72,11 @@ static __device__ __forceinline__ void prefetch_q_rows(const DecodeParams &p, in
         const int row_g = rb * kRowsPerBlock + half * 64 + i;
         if (row_g >= p.rows) break;
         const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
+#if MLA_F8
+        const uint8_t *row8 = p.q8 + (int64_t)b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2;
+        if ((reinterpret_cast<uintptr_t>(row8) & 15u) == 0) bulk_prefetch_l2(row8, kDqk);   // the 576-byte e4m3 row
+        continue;
+#endif
         const uint16_t *row = p.q + (int64_t)b * p.q_s0 + (int64_t)qi * p.q_s1 + (int64_t)qh * p.q_s2;
         if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0) continue;
         if (p.q_concat) {

@@ -192,6 +192,23 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
+// The same two forms with e4m3 operands (kind::f8f6f4, K = 32 per instruction).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
 // Arrive (once) on a local mbarrier when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -238,6 +255,17 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N, b
          | ((M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A/B (format code 0) and fp32 D.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+    return (1u << 4)                       // D: f32
+         | (0u << 7)                       // A: e4m3
+         | (0u << 10)                      // B: e4m3
+         | ((a_mn ? 1u : 0u) << 15)
+         | ((b_mn ? 1u : 0u) << 16)
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);
+}
+
 // Byte offset of element (row, chunk16) inside a K-major swizzled tile whose
 // rows are `row_bytes` long (128 for SW128, 64 for SW64), as TMA writes it
 // and as the tensor core reads it: the 16-byte chunk index is XORed with the
@@ -247,6 +275,10 @@ __host__ __device__ constexpr uint32_t swz128_offset(uint32_t row, uint32_t chun
 }
 __host__ __device__ constexpr uint32_t swz64_offset(uint32_t row, uint32_t chunk) {
     return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+}
+// 32-byte rows (SW32): the chunk index is XORed with address bit 7 (row bit 2).
+__host__ __device__ constexpr uint32_t swz32_offset(uint32_t row, uint32_t chunk) {
+    return row * 32u + ((chunk ^ ((row >> 2) & 1u)) << 4);
 }
 
 // ----------------------------------------------------------------------------
@@ -267,6 +299,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+// Four floats -> four e4m3 codes (round to nearest even, saturating to +-448),
+// a in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

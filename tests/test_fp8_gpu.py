@@ -1,0 +1,138 @@
+"""GPU parity of the e4m3 decode (mla_decode_fwd_fp8) against the fp64 oracle.
+
+The kernel rounds the probabilities to e4m3 for the PV product (round to
+nearest even: relative error at most 2^-4, roughly uniform, standard
+deviation ~0.036) while the denominator sums them unrounded, so the output
+error of element (row, d) is about bmm2_scale * sum_t delta_t w_t v_t[d] with
+independent delta_t: its standard deviation is ~0.036 * bmm2_scale *
+sqrt(sum_t w_t^2 v_t[d]^2), w the exact softmax weights (oracle).  The bar is
+eight of those, plus the bf16 rounding of the output (2^-8 |ref|) and 2e-3
+for probabilities that fall into e4m3's subnormal range.  The lse does not
+see the rounding: |lse - ref| <= 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import fp8 as F
+from oracle import reference as R
+from tests.parity import sample_rows
+
+pytestmark = pytest.mark.gpu
+
+BMM1, BMM2 = 0.8 / 24, 1.5
+SIGMA_REL = 0.036
+LSE_ATOL = 2e-3
+
+
+def _inputs(name, s_q, h_q, Ls, h_k=1, causal=False, seed=1):
+    w = workloads.Workload(name, batch=len(Ls), s_q=s_q, h_q=h_q, h_k=h_k, causal=causal,
+                           seqlens=("fixed", tuple(Ls)))
+    inp = workloads.make_inputs(w, seed=seed, poison=True)
+    return inp, workloads.e4m3_codes(inp.q), workloads.e4m3_codes(inp.k_cache)
+
+
+def _run(inp, q8, k8, parts=None):
+    import paged_mla_decode_10_gb300 as M
+    w = inp.workload
+    L, bt = inp.cache_seqlens.cuda(), inp.block_table.cuda()
+    md, ns = M.mla_get_metadata(L, w.rows, w.h_k, num_sm_parts=parts)
+    out, lse = M.mla_decode_fwd_fp8(q8.cuda(), k8.cuda(), bt, L, 512, md, ns, BMM1, BMM2, causal=w.causal)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _sigma(inp, q8, k8, rows):
+    """sqrt(sum_t w_t^2 v_t^2) per (row, dim), exact weights from the decoded values."""
+    w = inp.workload
+    B, s_q, h_q, _ = q8.shape
+    hpk = h_q // w.h_k
+    qv = F.e4m3_decode(q8.numpy())
+    kv = F.e4m3_decode(k8.numpy())
+    bt = inp.block_table.numpy()
+    L = inp.cache_seqlens.numpy()
+    out = np.zeros((len(rows), 512))
+    for n_r, row in enumerate(rows):
+        b, rem = divmod(int(row), s_q * h_q)
+        i, h = divmod(rem, h_q)
+        n = R.visible_keys(int(L[b]), s_q, i, w.causal)
+        if n == 0:
+            continue
+        t = np.arange(n)
+        K = kv[bt[b, t // 64], t % 64, h // hpk]          # (n, 576)
+        s = BMM1 * (K @ qv[b, i, h])
+        wts = np.exp(s - s.max())
+        wts /= wts.sum()
+        out[n_r] = np.sqrt((wts[:, None] ** 2 * K[:, :512] ** 2).sum(axis=0))
+    return out
+
+
+def _check(inp, q8, k8, out, lse, rows=None, where=""):
+    w = inp.workload
+    B, s_q, h_q, _ = q8.shape
+    if rows is None:
+        rows = list(range(B * s_q * h_q))
+    ref_o, ref_l = F.mla_decode_fp8(q8, k8, inp.block_table, inp.cache_seqlens, BMM1, BMM2, w.causal, rows=rows)
+    o = out.float().cpu().numpy().astype(np.float64).reshape(-1, 512)[rows]
+    ro = ref_o.reshape(-1, 512)[rows]
+    assert np.isfinite(o).all(), f"{where}: non-finite output"
+    bound = 8 * SIGMA_REL * BMM2 * _sigma(inp, q8, k8, rows) + 2.0 ** -8 * np.abs(ro) + 2e-3
+    err = np.abs(o - ro)
+    bad = err > bound
+    assert not bad.any(), (f"{where}: {bad.sum()} of {bad.size} outside the bar; first at "
+                           f"{tuple(np.argwhere(bad)[0])}: gpu {o[bad][0]} ref {ro[bad][0]} bound {bound[bad][0]}")
+    lf = lse.float().cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)[rows]
+    rl = ref_l.transpose(0, 2, 1).reshape(-1)[rows]
+    both = np.isneginf(lf) & np.isneginf(rl)
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both, 0.0, np.abs(lf - rl))
+    assert (lerr <= LSE_ATOL).all(), f"{where}: lse max err {lerr.max()}"
+    # the error is dominated by the P rounding, not by a systematic fault: its
+    # mean over the elements stays well inside the per-element bar
+    assert err.mean() < 0.25 * bound.mean(), f"{where}: mean err {err.mean()} vs mean bar {bound.mean()}"
+
+
+@pytest.mark.parametrize("parts", [None, 3])
+@pytest.mark.parametrize("case", [
+    ("h16_tiny", 1, 16, [100, 257], 1, False),
+    ("h128_ragged", 1, 128, [1, 63, 64, 65, 200, 1000], 1, False),
+    ("mtp_causal_small", 2, 128, [2, 64, 333, 1024], 1, True),
+    ("gqa_hk2", 1, 32, [90, 513], 2, False),
+])
+def test_fp8_small_cases(case, parts):
+    name, s_q, h_q, Ls, h_k, causal = case
+    inp, q8, k8 = _inputs(name, s_q, h_q, Ls, h_k=h_k, causal=causal, seed=len(Ls) * 13 + h_q)
+    out, lse = _run(inp, q8, k8, parts)
+    _check(inp, q8, k8, out, lse, where=f"{name} parts={parts}")
+
+
+def test_fp8_empty_and_invisible_rows():
+    inp, q8, k8 = _inputs("edge", 3, 16, [0, 1, 130], causal=True, seed=4)
+    out, lse = _run(inp, q8, k8, parts=2)
+    _check(inp, q8, k8, out, lse, where="edge")
+    assert (out[0] == 0).all() and torch.isinf(lse[0]).all()
+
+
+def test_fp8_dsv3_decode_sampled_rows():
+    inp = workloads.make_inputs("dsv3_decode", poison=True)
+    q8, k8 = workloads.e4m3_codes(inp.q), workloads.e4m3_codes(inp.k_cache)
+    out, lse = _run(inp, q8, k8)
+    rows = sample_rows(inp, 24, seed=5)
+    _check(inp, q8, k8, out, lse, rows=rows, where="dsv3_decode e4m3")
+
+
+def test_fp8_rejects_bad_scales_and_strides():
+    import paged_mla_decode_10_gb300 as M
+    inp, q8, k8 = _inputs("args", 1, 16, [70], seed=2)
+    L, bt = inp.cache_seqlens.cuda(), inp.block_table.cuda()
+    md, ns = M.mla_get_metadata(L, 16, 1)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        with pytest.raises(M.MlaError):
+            M.mla_decode_fwd_fp8(q8.cuda(), k8.cuda(), bt, L, 512, md, ns, bad, 1.0)
+    with pytest.raises(M.MlaError):
+        M.mla_decode_fwd_fp8(q8.cuda(), k8.cuda(), bt, L, 512, md, ns, BMM1, float("nan"))
+    q_pad = torch.zeros(1, 1, 16, 584, dtype=torch.uint8, device="cuda")[..., :576]   # head stride 584: not 16-aligned
+    q_pad.copy_(q8.cuda())
+    with pytest.raises(M.MlaError):
+        M.mla_decode_fwd_fp8(q_pad, k8.cuda(), bt, L, 512, md, ns, BMM1, 1.0)

@@ -192,6 +192,18 @@ def make_inputs(w: Workload | str, seed: Optional[int] = None, device="cpu",
     return Inputs(w, q, k, bt.to(device), L.to(device), scale, seed)
 
 
+def e4m3_codes(t: torch.Tensor, chunk: int = 1 << 24) -> torch.Tensor:
+    """The e4m3 codes (uint8, same shape and device) of a bf16 input tensor,
+    rounded by torch's float8_e4m3fn conversion; NaN stays NaN (0x7f).  Used
+    to draw e4m3 query and cache inputs from the seeded bf16 ones."""
+    out = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+    src, dst = t.reshape(-1), out.view(-1)
+    for s in range(0, src.numel(), chunk):
+        e = min(src.numel(), s + chunk)
+        dst[s:e] = src[s:e].float().to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
 def poison_unused(k_cache: torch.Tensor, block_table: torch.Tensor, seqlens: torch.Tensor):
     """Write NaN into every cache row that no sequence may read."""
     bt = block_table.cpu()
