@@ -57,16 +57,17 @@ def visible(L, s_q, i, causal):
     return max(0, min(L, n))
 
 
-def algorithmic_work(w: workloads.Workload, seqlens):
+def algorithmic_work(w: workloads.Workload, seqlens, elem=2):
     """(bytes, flops) one decode call must move / compute.
 
-    bytes: every valid cache row once (576 bf16 per KV head; V aliases K),
-    q, out (bf16), softmax_lse (fp32), the block_table entries used, seqlens.
+    bytes: every valid cache row once (576 elements of `elem` bytes per KV
+    head -- 2 for bf16, 1 for e4m3; V aliases K), q (same element size), out
+    (bf16), softmax_lse (fp32), the block_table entries used, seqlens.
     flops: 2 * (576 + 512) per (query row, visible key)."""
     Ls = [max(0, int(x)) for x in seqlens]
     B = len(Ls)
-    kv = sum(Ls) * w.h_k * 576 * 2
-    io = B * w.s_q * w.h_q * (576 * 2 + 512 * 2 + 4)
+    kv = sum(Ls) * w.h_k * 576 * elem
+    io = B * w.s_q * w.h_q * (576 * elem + 512 * 2 + 4)
     bt = sum((L + 63) // 64 for L in Ls) * 4 + B * 4
     vis = sum(visible(L, w.s_q, i, w.causal) for L in Ls for i in range(w.s_q))
     return kv + io + bt, 2.0 * (576 + 512) * w.h_q * vis
@@ -84,7 +85,8 @@ def load_peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("decode_splitkv.cu", "sm103.cuh", "decode_common.cuh", "decode_sync.cuh", "decode_epilogue.cuh", "tmem_ldst.inc"):
+    for f in ("decode_splitkv.cu", "decode_splitkv_fp8.cu", "sm103.cuh", "decode_common.cuh", "decode_sync.cuh",
+              "decode_epilogue.cuh", "tmem_ldst.inc"):
         with open(os.path.join(ROOT, "paged_mla_decode_10_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -92,7 +94,8 @@ def kernel_source_sha():
 
 def recorded_traffic(workload: str):
     """DRAM bytes per split-KV launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    taken on the current kernel source; else None.  Keys: the workload name
+    (bf16 kernel) or "<workload>@e4m3"."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -188,11 +191,17 @@ def oracle_sample(inp_cpu, target_flop, seed=0):
 SINGLE_THREAD_FLOP = 1e9
 
 
-def time_oracle(inp_cpu, rows, threads=0):
+def time_oracle(inp_cpu, rows, threads=0, e4m3=None):
+    """Seconds of one oracle call on `rows`; with e4m3 = (q codes, cache codes) the e4m3 oracle."""
     from oracle import reference as R
     t0 = time.perf_counter()
-    R.mla_decode(inp_cpu.q, inp_cpu.k_cache, inp_cpu.block_table, inp_cpu.cache_seqlens, 512, inp_cpu.scale,
-                 inp_cpu.workload.causal, rows=rows, threads=threads)
+    if e4m3 is not None:
+        from oracle import fp8 as F
+        F.mla_decode_fp8(e4m3[0], e4m3[1], inp_cpu.block_table, inp_cpu.cache_seqlens, inp_cpu.scale, 1.0,
+                         inp_cpu.workload.causal, rows=rows, threads=threads)
+    else:
+        R.mla_decode(inp_cpu.q, inp_cpu.k_cache, inp_cpu.block_table, inp_cpu.cache_seqlens, 512, inp_cpu.scale,
+                     inp_cpu.workload.causal, rows=rows, threads=threads)
     return time.perf_counter() - t0
 
 
@@ -248,13 +257,15 @@ def run_reference(args, w, world, rank):
     from oracle import reference as R
     inp = workloads.make_inputs(w, seed=workloads.seed_for(w.name), device="cpu", poison=False)
     L = inp.cache_seqlens.tolist()
-    nbytes, flop_total = algorithmic_work(w, L)
+    e4m3 = args.kv_dtype == "e4m3"
+    codes = (workloads.e4m3_codes(inp.q), workloads.e4m3_codes(inp.k_cache)) if e4m3 else None
+    nbytes, flop_total = algorithmic_work(w, L, 1 if e4m3 else 2)
     per_step_s = max(0.5, min(20.0, args.reference_budget_s / max(1, args.steps + args.warmup)))
     target = calibrate_target(per_step_s)
     rows, flop = oracle_sample(inp, target)
     for _ in range(args.warmup):
-        time_oracle(inp, rows)
-    ts = [time_oracle(inp, rows) for _ in range(args.steps)]
+        time_oracle(inp, rows, e4m3=codes)
+    ts = [time_oracle(inp, rows, e4m3=codes) for _ in range(args.steps)]
     t = sum(ts) / len(ts)
     us = t * (flop_total / flop) * 1e6
     cores = R.max_threads()
@@ -262,7 +273,7 @@ def run_reference(args, w, world, rank):
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, L, inp.seed, world),
+        "config": config_of(w, L, inp.seed, world, {"kv_dtype": args.kv_dtype}),
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{len(rows)} of {w.batch * w.s_q * w.h_q} query rows "
                                    f"({flop / 1e9:.2f} of {flop_total / 1e9:.1f} GFLOP), scaled by FLOPs"},
@@ -280,7 +291,12 @@ def run_libmla(args, w, world, rank, local):
     seed = workloads.seed_for(w.name) + 1000 * rank
     inp = workloads.make_inputs(w, seed=seed, device=dev, poison=False)
     L = inp.cache_seqlens.cpu().tolist()
-    nbytes, flop = algorithmic_work(w, L)
+    e4m3 = args.kv_dtype == "e4m3"
+    if e4m3:   # the same seeded draws rounded to e4m3; bmm1_scale = the softmax scale, bmm2_scale = 1
+        q_in, k_in = workloads.e4m3_codes(inp.q), workloads.e4m3_codes(inp.k_cache)
+    else:
+        q_in, k_in = inp.q, inp.k_cache
+    nbytes, flop = algorithmic_work(w, L, 1 if e4m3 else 2)
     peaks, peaks_src = load_peaks()
     stream = torch.cuda.current_stream(dev)
 
@@ -288,14 +304,20 @@ def run_libmla(args, w, world, rank, local):
     md, ns = M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=parts)
     out = torch.empty(w.batch, w.s_q, w.h_q, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.batch, w.h_q, w.s_q, dtype=torch.float32, device=dev)
-    shape = M.make_shape(inp.q, inp.k_cache, inp.block_table, out.stride()[:3], parts, 512)
+    shape = M.make_shape(q_in, k_in, inp.block_table, out.stride()[:3], parts, 512)
     ws = torch.empty(M.mla_workspace_size(shape), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     call = dict(softmax_scale=inp.scale, causal=w.causal, out=out, softmax_lse=lse, workspace=ws)
     args_kv = (inp.q, inp.k_cache, inp.block_table, inp.cache_seqlens, 512, md, ns)
 
+    args_f8 = (q_in, k_in, inp.block_table, inp.cache_seqlens, 512, md, ns, inp.scale, 1.0)
+    call_f8 = dict(causal=w.causal, out=out, softmax_lse=lse, workspace=ws)
+
     def decode():
-        M.mla_decode_fwd(*args_kv, **call)
+        if e4m3:
+            M.mla_decode_fwd_fp8(*args_f8, **call_f8)
+        else:
+            M.mla_decode_fwd(*args_kv, **call)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -338,7 +360,10 @@ def run_libmla(args, w, world, rank, local):
     for i in range(args.steps):
         flush.zero_()
         ev3[i][0].record(stream)
-        M.mla_decode_splitkv(*args_kv, **call)
+        if e4m3:
+            M.mla_decode_splitkv_fp8(*args_f8, **call_f8)
+        else:
+            M.mla_decode_splitkv(*args_kv, **call)
         ev3[i][1].record(stream)
         M.mla_decode_combine(*args_kv, **call)
         ev3[i][2].record(stream)
@@ -371,16 +396,19 @@ def run_libmla(args, w, world, rank, local):
     if bits:
         raise RuntimeError(f"device error bits {bits} during the benchmark")
 
+    # the tensor peak of the products' type: e4m3 = the measured bf16 peak x the nominal
+    # dense fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s)
+    tc_peak = peaks["bf16_tflops"] * (2.0 if e4m3 else 1.0)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flop / (peaks["bf16_tflops"] * 1e12)
+    t_tc = flop / (tc_peak * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     if bound == "hbm":
         achieved = nbytes / (kernel_ms * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
     else:
         achieved = flop / (kernel_ms * 1e-3) / 1e12
-        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    traffic = recorded_traffic(w.name)
+        peak, unit = tc_peak, "TFLOP/s"
+    traffic = recorded_traffic(w.name + ("@e4m3" if e4m3 else ""))
 
     # ---- e2e: one host-buffer call per step (copies in, schedule, decode, results back in host memory)
     q_h = inp.q.cpu().pin_memory()
@@ -389,9 +417,23 @@ def run_libmla(args, w, world, rank, local):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
-    def e2e_step():
-        M.mla_decode_fwd_host(q_h, inp.k_cache, bt_h, L_h, 512, softmax_scale=inp.scale, causal=w.causal,
-                              num_sm_parts=parts, out=out_h, softmax_lse=lse_h)
+    if e4m3:
+        # no host-buffer call for e4m3: the public calls with the copies around them, on the stream
+        q_h = q_in.cpu().pin_memory()
+        q_d, bt_d, L_d = torch.empty_like(q_in), torch.empty_like(inp.block_table), torch.empty_like(inp.cache_seqlens)
+
+        def e2e_step():
+            q_d.copy_(q_h, non_blocking=True)
+            bt_d.copy_(bt_h, non_blocking=True)
+            L_d.copy_(L_h, non_blocking=True)
+            md_d, ns_d = M.mla_get_metadata(L_d, w.rows, w.h_k, num_sm_parts=parts)
+            M.mla_decode_fwd_fp8(q_d, k_in, bt_d, L_d, 512, md_d, ns_d, inp.scale, 1.0, **call_f8)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+    else:
+        def e2e_step():
+            M.mla_decode_fwd_host(q_h, inp.k_cache, bt_h, L_h, 512, softmax_scale=inp.scale, causal=w.causal,
+                                  num_sm_parts=parts, out=out_h, softmax_lse=lse_h)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -406,7 +448,7 @@ def run_libmla(args, w, world, rank, local):
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev2) / args.steps, world, dev)
     if not (torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())):
         raise RuntimeError("the host-buffer call returned a different result from the device call")
-    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + L_h.numel() * 4
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + L_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
@@ -416,13 +458,14 @@ def run_libmla(args, w, world, rank, local):
         inp_cpu = inp.to("cpu")
         target = calibrate_target(args.cpu_seconds)
         rows, sflop = oracle_sample(inp_cpu, target)
-        t = time_oracle(inp_cpu, rows)
+        codes = (q_in.cpu(), k_in.cpu()) if e4m3 else None
+        t = time_oracle(inp_cpu, rows, e4m3=codes)
         cpu = {"value": t * (flop / sflop) * 1e6, "unit": UNIT, "cores": R.max_threads(), "kind": "oracle",
                "sample": f"{len(rows)} of {w.batch * w.s_q * w.h_q} query rows ({sflop / 1e9:.2f} of "
                          f"{flop / 1e9:.1f} GFLOP, {t:.1f} s), scaled to one call by FLOPs"}
         if flop <= SINGLE_THREAD_FLOP:
             # a workload small enough for one core: the whole call, single-threaded
-            cpu["single_thread_us"] = time_oracle(inp_cpu, None, threads=1) * 1e6
+            cpu["single_thread_us"] = time_oracle(inp_cpu, None, threads=1, e4m3=codes) * 1e6
 
     if rank != 0:
         return 0
@@ -432,13 +475,18 @@ def run_libmla(args, w, world, rank, local):
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q and cache, random page permutation)",
-        "config": config_of(w, L, seed, world, {"num_sm_parts": parts, "splits_total": int(ns[-1].item())}),
+        "dtype": "e4m3" if e4m3 else "bf16",
+        "data": ("synthetic (seeded N(0,1) q and cache rounded to e4m3, bmm1_scale = 1/24, bmm2_scale = 1, "
+                 "random page permutation)" if e4m3 else
+                 "synthetic (seeded N(0,1) bf16 q and cache, random page permutation)"),
+        "config": config_of(w, L, seed, world, {"num_sm_parts": parts, "splits_total": int(ns[-1].item()),
+                                                "kv_dtype": args.kv_dtype}),
         "achieved": {"hbm_tb_s": call_tbs, "tflop_s": call_tflops,
                      "roofline_us": max(t_hbm, t_tc) * 1e6,
                      "frac_of_roofline": max(t_hbm, t_tc) / (ms_per_step * 1e-3),
                      "algorithmic_bytes": nbytes, "algorithmic_flop": flop},
-        "roofline": {"bound": bound, "kernel": "mla_splitkv_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": bound, "kernel": "mla_splitkv_kernel_f8" if e4m3 else "mla_splitkv_kernel",
+                     "achieved": achieved, "peak": peak,
                      "unit": unit, "frac": achieved / peak, "traffic": traffic, "peak_source": peaks_src,
                      "kernel_us": kernel_ms * 1e3, "combine_us": combine_ms * 1e3,
                      "algorithmic_per_launch": nbytes if bound == "hbm" else flop},
@@ -463,6 +511,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget for cpu_baseline")
     ap.add_argument("--reference-budget-s", type=float, default=150.0, help="total oracle time of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",
+                    help="bf16: mla_decode_fwd; e4m3: mla_decode_fwd_fp8 on the same draws rounded to e4m3")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

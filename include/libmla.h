@@ -294,6 +294,19 @@ int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_ca
                        void *workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * The first of the two launches of mla_decode_fwd_fp8 (the e4m3 split-KV
+ * decode), with its arguments; the second is mla_decode_combine on the same
+ * workspace, which merges split sequences exactly as for bf16 inputs (the
+ * partials already carry bmm2_scale).  A NULL workspace selects the same
+ * internal one for both calls on one stream.
+ */
+int mla_decode_splitkv_fp8(const mla_shape_t *shape, const void *q, const void *k_cache,
+                           const int32_t *block_table, const int32_t *cache_seqlens,
+                           const int32_t *tile_scheduler_metadata, const int32_t *num_splits,
+                           float bmm1_scale, float bmm2_scale, int causal, void *out, float *softmax_lse,
+                           void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * One whole decode step from host buffers: copies q, block_table and
  * cache_seqlens to the device, computes the schedule (mla_get_metadata with
  * shape->num_sm_parts parts), decodes (mla_decode_fwd) and returns out and

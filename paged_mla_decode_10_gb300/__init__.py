@@ -22,6 +22,7 @@ from .api import (  # noqa: E402
     mla_decode_fwd_host,
     mla_decode_fwd_split,
     mla_decode_splitkv,
+    mla_decode_splitkv_fp8,
     mla_get_metadata,
     mla_get_num_sm_parts,
     mla_shutdown,
@@ -32,6 +33,6 @@ from ._lib import MlaError, MlaRopeStrides, MlaShape  # noqa: E402
 __all__ = [
     "HEAD_DIM", "HEAD_DIM_V", "PAGE_BLOCK_SIZE", "MlaError", "MlaRopeStrides", "MlaShape",
     "flash_mla_with_kvcache", "get_mla_metadata", "make_shape", "mla_check_device_error",
-    "mla_decode_combine", "mla_decode_fwd", "mla_decode_fwd_fp8", "mla_decode_fwd_host", "mla_decode_fwd_split", "mla_decode_splitkv", "mla_get_metadata",
+    "mla_decode_combine", "mla_decode_fwd", "mla_decode_fwd_fp8", "mla_decode_fwd_host", "mla_decode_fwd_split", "mla_decode_splitkv", "mla_decode_splitkv_fp8", "mla_get_metadata",
     "mla_get_num_sm_parts", "mla_shutdown", "mla_workspace_size",
 ]

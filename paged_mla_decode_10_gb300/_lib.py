@@ -83,9 +83,10 @@ def load():
     L.mla_decode_fwd_split.argtypes = [sp, ctypes.POINTER(MlaRopeStrides), vp, vp, vp, vp, vp, vp, vp, vp,
                                        ctypes.c_float, c_int, vp, vp, vp, c_size, vp]
     L.mla_decode_fwd_split.restype = c_int
-    L.mla_decode_fwd_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, c_int, vp, vp, vp,
+    for name in ("mla_decode_fwd_fp8", "mla_decode_splitkv_fp8"):
+        getattr(L, name).argtypes = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, c_int, vp, vp, vp,
                                      c_size, vp]
-    L.mla_decode_fwd_fp8.restype = c_int
+        getattr(L, name).restype = c_int
     L.mla_decode_fwd_host.argtypes = [sp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp]
     L.mla_decode_fwd_host.restype = c_int
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]

@@ -205,6 +205,22 @@ def mla_decode_fwd_fp8(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_
     """mla_decode_fwd over an e4m3 query (B, s_q, h_q, 576) and latent cache (num_blocks, 64, h_k, 576),
     given as float8_e4m3fn or uint8 (the e4m3 bytes) CUDA tensors, with the fused product scales:
     logits = bmm1_scale * q.k, out = bmm2_scale * softmax(logits) V.  Returns (out bf16, softmax_lse fp32)."""
+    return _decode_fp8("mla_decode_fwd_fp8", q, k_cache, block_table, cache_seqlens, head_dim_v,
+                       tile_scheduler_metadata, num_splits, bmm1_scale, bmm2_scale, causal, out, softmax_lse,
+                       workspace, stream)
+
+
+def mla_decode_splitkv_fp8(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_scheduler_metadata, num_splits,
+                           bmm1_scale, bmm2_scale=1.0, causal=False, out=None, softmax_lse=None, workspace=None,
+                           stream=None):
+    """First launch of mla_decode_fwd_fp8 (the e4m3 split-KV decode); mla_decode_combine is the second."""
+    return _decode_fp8("mla_decode_splitkv_fp8", q, k_cache, block_table, cache_seqlens, head_dim_v,
+                       tile_scheduler_metadata, num_splits, bmm1_scale, bmm2_scale, causal, out, softmax_lse,
+                       workspace, stream)
+
+
+def _decode_fp8(name, q, k_cache, block_table, cache_seqlens, head_dim_v, tile_scheduler_metadata, num_splits,
+                bmm1_scale, bmm2_scale, causal, out, softmax_lse, workspace, stream):
     L = _lib.load()
     _require(q.dim() == 4 and k_cache.dim() == 4, "q and k_cache must be 4-D")
     _require(q.dtype in _E4M3 and k_cache.dtype in _E4M3 and q.is_cuda and k_cache.is_cuda,
@@ -223,10 +239,10 @@ def mla_decode_fwd_fp8(q, k_cache, block_table, cache_seqlens, head_dim_v, tile_
     need = mla_workspace_size(sh)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    check(L.mla_decode_fwd_fp8(ctypes.byref(sh), _ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(cache_seqlens),
-                               _ptr(tile_scheduler_metadata), _ptr(num_splits), float(bmm1_scale), float(bmm2_scale),
-                               int(bool(causal)), _ptr(out), _ptr(softmax_lse), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream)), "mla_decode_fwd_fp8")
+    check(getattr(L, name)(ctypes.byref(sh), _ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(cache_seqlens),
+                           _ptr(tile_scheduler_metadata), _ptr(num_splits), float(bmm1_scale), float(bmm2_scale),
+                           int(bool(causal)), _ptr(out), _ptr(softmax_lse), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)), name)
     return out, softmax_lse
 
 

@@ -650,10 +650,15 @@ int mla_decode_fwd(const mla_shape_t *shape, const void *q, const void *k_cache,
     return launch_combine(shape, pr, s);
 }
 
-int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
-                       const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float bmm1_scale,
-                       float bmm2_scale, int causal, void *out, float *lse, void *ws, size_t ws_bytes,
-                       mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Validation and launches of the e4m3 decode; `combine` selects both launches
+// (mla_decode_fwd_fp8) or the split-KV one alone (mla_decode_splitkv_fp8).
+int decode_fp8(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+               const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float bmm1_scale,
+               float bmm2_scale, int causal, void *out, float *lse, void *ws, size_t ws_bytes, mla_stream_t stream,
+               bool combine) {
     int st = check_args(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, out, lse, true);
     if (st != MLA_OK) return st;
     if (!(bmm1_scale > 0.f) || !std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale))
@@ -679,7 +684,26 @@ int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_ca
     src.elem = 1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if ((st = launch_splitkv(shape, src, pr, s)) != MLA_OK) return st;
-    return launch_combine(shape, pr, s);
+    return combine ? launch_combine(shape, pr, s) : MLA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_cache, const int32_t *block_table,
+                       const int32_t *cache_seqlens, const int32_t *md, const int32_t *num_splits, float bmm1_scale,
+                       float bmm2_scale, int causal, void *out, float *lse, void *ws, size_t ws_bytes,
+                       mla_stream_t stream) {
+    return decode_fp8(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, bmm1_scale, bmm2_scale, causal,
+                      out, lse, ws, ws_bytes, stream, true);
+}
+
+int mla_decode_splitkv_fp8(const mla_shape_t *shape, const void *q, const void *k_cache,
+                           const int32_t *block_table, const int32_t *cache_seqlens, const int32_t *md,
+                           const int32_t *num_splits, float bmm1_scale, float bmm2_scale, int causal, void *out,
+                           float *lse, void *ws, size_t ws_bytes, mla_stream_t stream) {
+    return decode_fp8(shape, q, k_cache, block_table, cache_seqlens, md, num_splits, bmm1_scale, bmm2_scale, causal,
+                      out, lse, ws, ws_bytes, stream, false);
 }
 
 int mla_decode_fwd_split(const mla_shape_t *shape, const mla_rope_strides_t *rope, const void *q_nope,
