@@ -88,24 +88,41 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kThreads = 320;                   // 10 warps, roles below
+// S/P buffers in TMEM and how far QK^T runs ahead of PV: two buffers (QK^T(i)
+// waits for PV(i - 2)) beside a 128-column bf16 Q; three beside the 64-column
+// e4m3 Q (QK^T(i) waits for PV(i - 3), PV issued two pages behind QK^T).
+#if MLA_F8
+constexpr int kSBufs = 3;
+constexpr int kPvBars = 2;   // PV completions alternate over two barriers (see the O correction)
+#else
+constexpr int kSBufs = 2;
+constexpr int kPvBars = 1;
+#endif
+constexpr int kLag = kSBufs - 1;                // PV(i) is issued after QK^T(i + kLag)
 
 // barrier indices
 constexpr int B_KFULL = 0;
 constexpr int B_KEMPTY = B_KFULL + kStages;
 constexpr int B_SFULL = B_KEMPTY + kStages;
-constexpr int B_SREAD = B_SFULL + 2;            // exchange warps have read S out of TMEM
-constexpr int B_PFULL = B_SREAD + 2;
-constexpr int B_XFULL = B_PFULL + 2;            // peer's partial tile has landed in XIN
+constexpr int B_SREAD = B_SFULL + kSBufs;       // exchange warps have read S out of TMEM
+constexpr int B_PFULL = B_SREAD + kSBufs;
+constexpr int B_XFULL = B_PFULL + kSBufs;       // peer's partial tile has landed in XIN
 constexpr int B_XINFREE = B_XFULL + 2;          // peer has read the tile we sent into its XIN slot
 constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received our last tile: XOUT reusable
-constexpr int B_PVDONE = B_STAGEFREE + 1;
-constexpr int B_OFINAL = B_PVDONE + 1;
+constexpr int B_PVDONE = B_STAGEFREE + 1;      // kPvBars of them, page i on PVDONE + i % kPvBars
+constexpr int B_OFINAL = B_PVDONE + kPvBars;
 constexpr int B_QREADY = B_OFINAL + 1;
 constexpr int B_DRAIN = B_QREADY + 1;
 constexpr int B_COUNT = B_DRAIN + 1;
 static_assert(B_COUNT <= 64, "barrier area");
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;
+// first TMEM column of S/P buffer sb: 256, 320 (and 448, after the e4m3 Q)
+#if MLA_F8
+__device__ __forceinline__ uint32_t s_col(uint32_t sb) { return sb == 2u ? 448u : TM_S + 64u * sb; }
+#else
+__device__ __forceinline__ uint32_t s_col(uint32_t sb) { return TM_S + 64u * sb; }
+#endif
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 // The CTA-scope acquire of wait_bar suffices for every barrier here: XFULL
@@ -171,8 +188,8 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
 // MMA issuer.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i, bool first_of_seg, int lane) {
-    const uint32_t st = i % kStages, pb = i & 1u;
-    bool ok = wait_bar(c, bar_addr(c, B_PFULL + pb), (i >> 1) & 1u);
+    const uint32_t st = i % kStages, pb = i % kSBufs;
+    bool ok = wait_bar(c, bar_addr(c, B_PFULL + pb), (i / kSBufs) & 1u);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return false;
     tc_fence_after();
@@ -181,21 +198,21 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
         constexpr uint32_t idPV = make_idesc_e4m3(128, 256, false, true);
         // V of this stage, MN-major: 2 boxes of 128 dims (LBO 8 KB), 8-key groups 1 KB apart
         const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
-        const uint32_t pa = tmem + TM_S + 64u * pb;   // P (e4m3 quads, 8 columns per 32 keys) where its S was
+        const uint32_t pa = tmem + s_col(pb);   // P (e4m3 quads, 8 columns per 32 keys) where its S was
         umma_ts_f8(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
         umma_ts_f8(tmem + TM_O, pa + 8u, bd0 + 256u, idPV, 1u);   // +32 keys = +4096 B
 #else
         constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
         // V of this stage, MN-major: 4 boxes of 64 dims (LBO 8 KB), 8-key groups 1 KB apart
         const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
-        const uint32_t pa = tmem + TM_S + 64u * pb;   // P (bf16 pairs, 8 columns per 16 keys) where its S was
+        const uint32_t pa = tmem + s_col(pb);   // P (bf16 pairs, 8 columns per 16 keys) where its S was
         umma_ts(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < 4; ++kk)   // +16 keys = +2048 B = +128 in the descriptor's 16-byte units
             umma_ts(tmem + TM_O, pa + 8u * kk, bd0 + 128u * kk, idPV, 1u);
 #endif
         umma_commit(bar_addr(c, B_KEMPTY + st));
-        umma_commit(bar_addr(c, B_PVDONE));
+        umma_commit(bar_addr(c, B_PVDONE + i % kPvBars));
     }
     __syncwarp();
     return true;
@@ -220,7 +237,7 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
         const int tail = s.L & (kPage - 1);
         const int n = s.hi - s.lo;
         for (int j = 0; j < n; ++j, ++it) {
-            const uint32_t st = it % kStages, sb = it & 1u;
+            const uint32_t st = it % kStages, sb = it % kSBufs;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (it / kStages) & 1u));
             if (!ok) break;
             const uint32_t stage = c.base + OFF_K + st * kHalfBytes;
@@ -239,11 +256,11 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // Buffer sb last held S/P of page it-2; PV(it-2) was issued before
+            // Buffer sb last held S/P of page it - kSBufs; its PV was issued before
             // this S (tcgen05 MMAs of one thread execute in issue order).
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t dS = tmem + TM_S + 64u * sb;
+                const uint32_t dS = tmem + s_col(sb);
                 // K-major page boxes: +32 B per 16-dim k-step, +8 KB per 64-dim box (16-byte units)
                 const uint64_t bk = make_sdesc(stage, 16, 1024, kSwizzle128B);
 #if MLA_F8
@@ -268,12 +285,17 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 umma_commit(bar_addr(c, B_SFULL + sb));
             }
             __syncwarp();
-            if (j > 0) {
-                if (!issue_pv(c, tmem, it - 1, j == 1, lane)) { ok = false; break; }
+            if (j >= kLag) {
+                if (!issue_pv(c, tmem, it - kLag, j == kLag, lane)) { ok = false; break; }
             }
         }
         if (!ok) break;
-        if (!issue_pv(c, tmem, it - 1, n == 1, lane)) { ok = false; break; }
+        // the segment's last kLag pages (page n - d is its first when n == d)
+#pragma unroll
+        for (int d = kLag; d >= 1; --d) {
+            if (n >= d && !issue_pv(c, tmem, it - d, n == d, lane)) { ok = false; break; }
+        }
+        if (!ok) break;
         if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
         __syncwarp();
         ++g;
@@ -401,20 +423,22 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     if (have) load_q_half(c, p, tmem_q, q, lane, rb, cta, hk, s);
     while (ok && have) {
         for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
+            // S/P buffer sb (phase phS); landing slot b of the peer (phase ph)
+            const uint32_t sb = it % kSBufs, phS = (it / kSBufs) & 1u;
             const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + b), ph));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
             if (!ok) break;
             if (!active) {
-                if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
+                if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
                 continue;
             }
             tc_fence_after();
             uint32_t raw[64];
-            tmem_ld_32x32b_x64(tmem + lane_base + TM_S + 64u * b, raw);
+            tmem_ld_32x32b_x64(tmem + lane_base + s_col(sb), raw);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + b));
+            if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
             if (!ok) break;
             // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
@@ -490,8 +514,10 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
         float m_ref = -INFINITY, l_sum = 0.f;
 
         for (int blk = s.lo; blk < s.hi && ok; ++blk, ++it) {
-            const uint32_t sb = it & 1u, ph = (it >> 1) & 1u;
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), ph));
+            // S/P buffer sb (phase phS); landing slot xb of the peer's tile (phase ph)
+            const uint32_t sb = it % kSBufs, phS = (it / kSBufs) & 1u;
+            const uint32_t xb = it & 1u, ph = (it >> 1) & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
             if (!ok) break;
             tc_fence_after();
             if (!warp_active) {
@@ -499,7 +525,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 uint32_t z[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[j] = 0u;
-                tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, z);
+                tmem_st_32x32b_x32(tmem + lane_base + s_col(sb), z);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar_addr(c, B_PFULL + sb));
@@ -508,26 +534,26 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             float sv[64];
             {
                 uint32_t raw[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + TM_S + 64u * sb, raw);
+                tmem_ld_32x32b_x64(tmem + lane_base + s_col(sb), raw);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
             }
             // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
             // add, then tell the peer its staging buffer (and our XIN slot) is free
-            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + sb), 8192u);
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + sb), ph));
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), 8192u);
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + xb), ph));
             if (!ok) break;
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
-                    smem_gen + ((sb ? xrow_local[1] : xrow_local[0]) - c.base) + (ch >> 3) * 4096 +
+                    smem_gen + ((xb ? xrow_local[1] : xrow_local[0]) - c.base) + (ch >> 3) * 4096 +
                     (((ch & 7) ^ (r & 7)) << 4));
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
             __syncwarp();
-            if ((r & 31) == 0) mbar_arrive_remote_relaxed(sb ? xfree_peer[1] : xfree_peer[0]);
+            if ((r & 31) == 0) mbar_arrive_remote_relaxed(xb ? xfree_peer[1] : xfree_peer[0]);
 
             // ---- mask (only pages the row does not see whole) + page max, on the raw
             // logits; the scale (> 0) is applied inside the exponent below
@@ -576,17 +602,20 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             l_sum += psum;
             // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
             // once the exchange warps have copied that S out
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), ph));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), phS));
             if (!ok) break;
             tc_fence_after();
 #if MLA_F8
-            tmem_st_32x32b_x16(tmem + lane_base + TM_S + 64u * sb, pk);
+            tmem_st_32x32b_x16(tmem + lane_base + s_col(sb), pk);
 #else
-            tmem_st_32x32b_x32(tmem + lane_base + TM_S + 64u * sb, pk);
+            tmem_st_32x32b_x32(tmem + lane_base + s_col(sb), pk);
 #endif
             // ---- lazy O correction, after PV(it - 1) has landed in TMEM
             if (__any_sync(0xffffffffu, raise && o_live)) {
-                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PVDONE), (it - 1) & 1u));
+                // PV(it - 1) on its barrier.  No phase alias: S(it) complete means
+                // QK^T(it) done, and it was issued after PV(it - kSBufs)
+                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_PVDONE + (it - 1) % kPvBars),
+                                                      ((it - 1) / kPvBars) & 1u));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -678,15 +707,17 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
             mbar_init(bar_addr(c, B_KFULL + i), 1);
             mbar_init(bar_addr(c, B_KEMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(bar_addr(c, B_SFULL + i), 1);
             mbar_init(bar_addr(c, B_SREAD + i), 4);
             mbar_init(bar_addr(c, B_PFULL + i), 128);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, B_XFULL + i), nwa);       // + 8 KB of DMA per arrival
             mbar_init(bar_addr(c, B_XINFREE + i), nwa);     // remote arrivals from the peer
         }
         mbar_init(bar_addr(c, B_STAGEFREE), nwa);           // remote arrivals from the peer
-        mbar_init(bar_addr(c, B_PVDONE), 1);
+        for (int i = 0; i < kPvBars; ++i) mbar_init(bar_addr(c, B_PVDONE + i), 1);
         mbar_init(bar_addr(c, B_OFINAL), 1);
         mbar_init(bar_addr(c, B_QREADY), 128);
         mbar_init(bar_addr(c, B_DRAIN), 1);
