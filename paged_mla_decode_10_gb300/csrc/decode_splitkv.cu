@@ -405,6 +405,13 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
+#if MLA_F8
+    // bf16 partial logits when more than 32 rows are exchanged (the DSMEM link then bounds the
+    // page rate); one warp's rows stay fp32 (there the softmax's conversions would cost more)
+    const bool xbf16 = p.rows - rb * kRowsPerBlock > 32;
+#else
+    constexpr bool xbf16 = false;
+#endif
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
@@ -441,6 +448,36 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
             if (!ok) break;
+#if MLA_F8
+            if (xbf16) {
+                // the partial logits rounded to bf16 (both CTAs then add bf16(S_0) + bf16(S_1),
+                // bitwise the same sum): 64 B per row and key half, [half][32 rows][64 B],
+                // 16-byte chunks swizzled by (row >> 1) & 3; keys 0-31 leave first
+                uint32_t wb[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) wb[j] = pack_bf16x2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1]));
+                uint8_t *mine = half0 - lane * 128 + lane * 64;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4 *>(mine + ((ch ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(wb[4 * ch], wb[4 * ch + 1], wb[4 * ch + 2], wb[4 * ch + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+                if (!ok) break;
+                const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
+                const uint32_t src = c.base + OFF_XOUT + (uint32_t)q * 8192u, dst = xin_peer + b * kXBytes;
+                if (lane == 0) bulk_copy_to_peer(dst, src, 2048u, xfull);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4 *>(mine + 2048 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(wb[16 + 4 * ch], wb[16 + 4 * ch + 1], wb[16 + 4 * ch + 2], wb[16 + 4 * ch + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) bulk_copy_to_peer(dst + 2048u, src + 2048u, 2048u, xfull);
+                continue;
+            }
+#endif
             // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
@@ -490,6 +527,13 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const int row_g = rb * kRowsPerBlock + r;  // row within the KV head's R rows
     const bool row_real = row_g < p.rows;
     const bool warp_active = rb * kRowsPerBlock + warp * 32 < p.rows;
+#if MLA_F8
+    // bf16 partial logits when more than 32 rows are exchanged (the DSMEM link then bounds the
+    // page rate); one warp's rows stay fp32 (there the softmax's conversions would cost more)
+    const bool xbf16 = p.rows - rb * kRowsPerBlock > 32;
+#else
+    constexpr bool xbf16 = false;
+#endif
     const int qi = row_g / p.hpk;              // query token i
     const int qh = hk * p.hpk + row_g % p.hpk; // query head h
     const uint32_t peer = (uint32_t)(cta ^ 1);
@@ -541,10 +585,29 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             }
             // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
             // add, then tell the peer its staging buffer (and our XIN slot) is free
-            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), 8192u);
+            // the peer's partial logits of the warp's 32 rows: 8 KB of fp32, or 4 KB of bf16
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), xbf16 ? 4096u : 8192u);
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + xb), ph));
             if (!ok) break;
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
+#if MLA_F8
+            if (xbf16) {
+                const uint8_t *xrow = smem_gen + OFF_XIN + xb * kXBytes + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 64u;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {   // keys 8ch .. 8ch + 7
+                    const uint4 t = *reinterpret_cast<const uint4 *>(xrow + (ch >> 2) * 2048 +
+                                                                     (((ch & 3) ^ ((r >> 1) & 3)) << 4));
+                    const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j = 8 * ch + 2 * k;
+                        const uint32_t own = pack_bf16x2(sv[j], sv[j + 1]);
+                        sv[j] = bf16lo_to_f32(own) + bf16lo_to_f32(tw[k]);
+                        sv[j + 1] = bf16hi_to_f32(own) + bf16hi_to_f32(tw[k]);
+                    }
+                }
+            } else
+#endif
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(

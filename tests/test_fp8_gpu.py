@@ -7,8 +7,12 @@ error of element (row, d) is about bmm2_scale * sum_t delta_t w_t v_t[d] with
 independent delta_t: its standard deviation is ~0.036 * bmm2_scale *
 sqrt(sum_t w_t^2 v_t[d]^2), w the exact softmax weights (oracle).  The bar is
 eight of those, plus the bf16 rounding of the output (2^-8 |ref|) and 2e-3
-for probabilities that fall into e4m3's subnormal range.  The lse does not
-see the rounding: |lse - ref| <= 2e-3.
+for probabilities that fall into e4m3's subnormal range.
+
+The pair of CTAs exchanges its two partial logit sums rounded to bf16 (both
+add bf16(S_0) + bf16(S_1)), which moves a logit by at most bmm1_scale *
+2^-9 * sum_d |q_d k_d| and the lse -- a smooth maximum of the logits -- by at
+most the largest such move over the row's keys: |lse - ref| <= 2e-3 + that.
 """
 import numpy as np
 import pytest
@@ -44,7 +48,8 @@ def _run(inp, q8, k8, parts=None):
 
 
 def _sigma(inp, q8, k8, rows):
-    """sqrt(sum_t w_t^2 v_t^2) per (row, dim), exact weights from the decoded values."""
+    """sqrt(sum_t w_t^2 v_t^2) per (row, dim), exact weights from the decoded values, and
+    per row the largest logit move the bf16 rounding of the partial sums allows."""
     w = inp.workload
     B, s_q, h_q, _ = q8.shape
     hpk = h_q // w.h_k
@@ -53,6 +58,7 @@ def _sigma(inp, q8, k8, rows):
     bt = inp.block_table.numpy()
     L = inp.cache_seqlens.numpy()
     out = np.zeros((len(rows), 512))
+    dlogit = np.zeros(len(rows))
     for n_r, row in enumerate(rows):
         b, rem = divmod(int(row), s_q * h_q)
         i, h = divmod(rem, h_q)
@@ -65,7 +71,8 @@ def _sigma(inp, q8, k8, rows):
         wts = np.exp(s - s.max())
         wts /= wts.sum()
         out[n_r] = np.sqrt((wts[:, None] ** 2 * K[:, :512] ** 2).sum(axis=0))
-    return out
+        dlogit[n_r] = BMM1 * 2.0 ** -9 * (np.abs(K) @ np.abs(qv[b, i, h])).max()
+    return out, dlogit
 
 
 def _check(inp, q8, k8, out, lse, rows=None, where=""):
@@ -77,7 +84,8 @@ def _check(inp, q8, k8, out, lse, rows=None, where=""):
     o = out.float().cpu().numpy().astype(np.float64).reshape(-1, 512)[rows]
     ro = ref_o.reshape(-1, 512)[rows]
     assert np.isfinite(o).all(), f"{where}: non-finite output"
-    bound = 8 * SIGMA_REL * BMM2 * _sigma(inp, q8, k8, rows) + 2.0 ** -8 * np.abs(ro) + 2e-3
+    sig, dlogit = _sigma(inp, q8, k8, rows)
+    bound = 8 * SIGMA_REL * BMM2 * sig + 2.0 ** -8 * np.abs(ro) + 2e-3
     err = np.abs(o - ro)
     bad = err > bound
     assert not bad.any(), (f"{where}: {bad.sum()} of {bad.size} outside the bar; first at "
@@ -87,7 +95,7 @@ def _check(inp, q8, k8, out, lse, rows=None, where=""):
     both = np.isneginf(lf) & np.isneginf(rl)
     with np.errstate(invalid="ignore"):
         lerr = np.where(both, 0.0, np.abs(lf - rl))
-    assert (lerr <= LSE_ATOL).all(), f"{where}: lse max err {lerr.max()}"
+    assert (lerr <= LSE_ATOL + dlogit).all(), f"{where}: lse max err {lerr.max()}"
     # the error is dominated by the P rounding, not by a systematic fault: its
     # mean over the elements stays well inside the per-element bar
     assert err.mean() < 0.25 * bound.mean(), f"{where}: mean err {err.mean()} vs mean bar {bound.mean()}"
@@ -99,6 +107,7 @@ def _check(inp, q8, k8, out, lse, rows=None, where=""):
     ("h128_ragged", 1, 128, [1, 63, 64, 65, 200, 1000], 1, False),
     ("mtp_causal_small", 2, 128, [2, 64, 333, 1024], 1, True),
     ("gqa_hk2", 1, 32, [90, 513], 2, False),
+    ("rows_40", 1, 40, [129, 64, 1000], 1, False),   # bf16 exchange with a partly filled second warp
 ])
 def test_fp8_small_cases(case, parts):
     name, s_q, h_q, Ls, h_k, causal = case
