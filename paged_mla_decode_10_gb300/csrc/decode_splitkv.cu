@@ -37,11 +37,17 @@
 // e4m3 variant.  The same source compiled with MLA_F8=1 (decode_splitkv_fp8.cu)
 // gives mla_splitkv_kernel_f8 for an e4m3 query and cache with the two fused
 // product scales of the FlashInfer page (trtllm_batch_decode_with_kv_cache_mla,
-// bmm1_scale / bmm2_scale note): the MMAs are kind::f8f6f4 (K = 32), a page
-// half is 18,432 B (two 128-dim SW128 boxes and one 32-byte SW32 RoPE box),
-// the ring has six stages, Q fills TMEM columns [384,448) (e4m3 quads), P is
-// rounded to e4m3 (quads, 16 columns) for the PV MMA while the denominator
-// sums the fp32 values, and the epilogue multiplies by bmm2_scale.
+// bmm1_scale / bmm2_scale note):
+//   - the MMAs are kind::f8f6f4 (K = 32): 9 per page for QK^T, 2 for PV;
+//   - a page half is 18,432 B (two 128-dim SW128 boxes and one 32-byte SW32
+//     RoPE box), so the ring has six stages;
+//   - Q fills TMEM columns [384,448) (e4m3 quads), which leaves [448,512) for
+//     a third S/P buffer: QK^T runs two pages ahead of PV;
+//   - with more than 32 rows the pair exchanges its partial logits as bf16
+//     and both CTAs add bf16(S_0) + bf16(S_1) (half the DSMEM bytes);
+//   - P is rounded to e4m3 (quads, 16 columns) for the PV MMA while the
+//     denominator sums the fp32 values, and the epilogue multiplies by
+//     bmm2_scale.
 //
 // Online softmax (log2 domain) with lazy rescaling: the running max is only
 // raised when a page's max exceeds it by more than 8 (a factor of 256), so
