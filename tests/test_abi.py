@@ -123,3 +123,23 @@ def test_split_decode_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call() == 1                                       # head stride below 64 dims
     rs.krope_stride[2] = 64
     assert call(shape=_shape(q_stride=(16 * 512, 16 * 512, 504), k_stride=(64 * 512, 512, 512))) == 1
+
+
+def test_fp8_decode_rejects_bad_arguments_before_any_cuda_call(lib):
+    dummy = ctypes.c_void_p(256)
+
+    def call(shape=None, q=dummy, bmm1=0.04, bmm2=1.0, fn="mla_decode_fwd_fp8"):
+        sh = shape or _shape()
+        return getattr(lib, fn)(ctypes.byref(sh), q, dummy, dummy, dummy, dummy, dummy, ctypes.c_float(bmm1),
+                                ctypes.c_float(bmm2), 0, dummy, dummy, dummy, 1 << 30, None)
+    for fn in ("mla_decode_fwd_fp8", "mla_decode_splitkv_fp8"):
+        assert call(q=None, fn=fn) == 1                                   # NULL q
+        assert call(q=ctypes.c_void_p(264), fn=fn) == 1                   # q not 16-byte aligned
+        for bad in (0.0, -1.0, float("nan"), float("inf")):
+            assert call(bmm1=bad, fn=fn) == 1                             # bmm1_scale not positive and finite
+        assert b"bmm1_scale" in lib.mla_last_error()
+        assert call(bmm2=float("nan"), fn=fn) == 1                        # bmm2_scale not finite
+        # a head stride of 584 bytes: a multiple of 8 elements but not of 16 bytes
+        assert call(shape=_shape(q_stride=(16 * 584, 16 * 584, 584)), fn=fn) == 1
+        assert b"16" in lib.mla_last_error()
+        assert call(shape=_shape(head_dim=512), fn=fn) == 1              # bad shape
