@@ -145,3 +145,29 @@ def test_fp8_rejects_bad_scales_and_strides():
     q_pad.copy_(q8.cuda())
     with pytest.raises(M.MlaError):
         M.mla_decode_fwd_fp8(q_pad, k8.cuda(), bt, L, 512, md, ns, BMM1, 1.0)
+
+
+def test_fp8_strided_inputs_match_contiguous_bitwise():
+    """Padded rows: q heads 592 bytes apart (not a multiple of 32: the Q loader's 16-byte path),
+    cache rows 640 bytes apart (the tensor maps' strides); same result bit for bit."""
+    inp, q8, k8 = _inputs("strided", 1, 128, [70, 300, 1000], seed=8)
+    out_c, lse_c = _run(inp, q8, k8)
+    qp = torch.zeros(*q8.shape[:3], 592, dtype=torch.uint8)
+    qp[..., :576] = q8
+    kp = torch.zeros(*k8.shape[:3], 640, dtype=torch.uint8)
+    kp[..., :576] = k8
+    q_s, k_s = qp.cuda()[..., :576], kp.cuda()[..., :576]
+    assert q_s.stride(2) == 592 and k_s.stride(1) == 640
+    import paged_mla_decode_10_gb300 as M
+    w = inp.workload
+    L, bt = inp.cache_seqlens.cuda(), inp.block_table.cuda()
+    md, ns = M.mla_get_metadata(L, w.rows, w.h_k)
+    out_s, lse_s = M.mla_decode_fwd_fp8(q_s, k_s, bt, L, 512, md, ns, BMM1, BMM2, causal=w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(out_s, out_c) and torch.equal(lse_s, lse_c)
+
+
+def test_fp8_single_part_is_unsplit():
+    inp, q8, k8 = _inputs("one_part", 1, 128, [1, 200, 1000], seed=9)
+    out, lse = _run(inp, q8, k8, parts=1)
+    _check(inp, q8, k8, out, lse, where="one part")
