@@ -6,8 +6,12 @@
  * |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 2e-3.
  *
  * Problem: batch 3, s_q 2 (causal), 16 query heads, 1 KV head, cache lengths
- * {100, 1, 300} in a pool of 9 shuffled 64-row blocks.  Exit status 0 on
- * success.
+ * {100, 1, 300} in a pool of 9 shuffled 64-row blocks.  The same values
+ * rounded to e4m3 then go through mla_decode_fwd_fp8 (bmm1_scale, bmm2_scale),
+ * held to the oracle on the decoded values with a coarse bar
+ * |out - ref| <= 0.03 + 0.03 |ref| (the probabilities are rounded to e4m3;
+ * the Python tests hold the derived bar), |lse - ref| <= 2e-3.  Exit status 0
+ * on success.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +48,29 @@ static float from_bf16(uint16_t h) {
     float f;
     memcpy(&f, &u, 4);
     return f;
+}
+/* e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; subnormals m * 2^-9;
+ * largest finite 448): round to nearest even, saturating; and back. */
+static uint8_t to_e4m3(float f) {
+    const uint8_t sign = signbit(f) ? 0x80 : 0;
+    double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                           /* subnormal range */
+        const double m = nearbyint(a * 512.0);          /* units of 2^-9, ties to even */
+        return sign | (uint8_t)(m >= 8.0 ? 0x08 : m);  /* 8 * 2^-9 is the smallest normal */
+    }
+    int e;
+    const double fr = frexp(a, &e);                     /* a = fr * 2^e, fr in [0.5, 1) */
+    e -= 1;                                             /* a = (2 fr) * 2^e, 2 fr in [1, 2) */
+    double m = nearbyint((2.0 * fr - 1.0) * 8.0);
+    if (m >= 8.0) { m = 0.0; e += 1; }
+    if (e > 8 || (e == 8 && m > 6.0)) return sign | 0x7E;
+    return sign | (uint8_t)((e + 7) << 3) | (uint8_t)m;
+}
+static float from_e4m3(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    const double mag = e == 0 ? m * ldexp(1.0, -9) : (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return (float)((c & 0x80) ? -mag : mag);
 }
 
 #define CUDA_OK(x) do { cudaError_t e_ = (x); if (e_ != cudaSuccess) { \
@@ -100,6 +127,25 @@ int main(void) {
     if (bits != 0) { fprintf(stderr, "device error bits %d\n", bits); return 4; }
     CUDA_OK(cudaMemcpy(out, out_d, (size_t)B * SQ * HQ * DV * 2, cudaMemcpyDeviceToHost));
     CUDA_OK(cudaMemcpy(lse, lse_d, (size_t)B * HQ * SQ * 4, cudaMemcpyDeviceToHost));
+
+    /* ---- the same values rounded to e4m3, through mla_decode_fwd_fp8 */
+    const float bmm1 = 0.8f / 24.0f, bmm2 = 1.5f;
+    uint8_t *q8 = malloc(nq), *k8 = malloc(nk);
+    uint16_t *q8v = malloc(nq * 2), *k8v = malloc(nk * 2), *out8 = malloc((size_t)B * SQ * HQ * DV * 2);
+    float *lse8 = malloc((size_t)B * HQ * SQ * 4);
+    for (size_t i = 0; i < nq; ++i) { q8[i] = to_e4m3(from_bf16(q[i])); q8v[i] = to_bf16(from_e4m3(q8[i])); }
+    for (size_t i = 0; i < nk; ++i) { k8[i] = to_e4m3(from_bf16(k[i])); k8v[i] = to_bf16(from_e4m3(k8[i])); }
+    void *q8_d, *k8_d;
+    CUDA_OK(cudaMalloc(&q8_d, nq));
+    CUDA_OK(cudaMalloc(&k8_d, nk));
+    CUDA_OK(cudaMemcpy(q8_d, q8, nq, cudaMemcpyHostToDevice));
+    CUDA_OK(cudaMemcpy(k8_d, k8, nk, cudaMemcpyHostToDevice));
+    MLA_OK_(mla_decode_fwd_fp8(&sh, q8_d, k8_d, bt_d, L_d, md_d, ns_d, bmm1, bmm2, 1, out_d, lse_d, NULL, 0, NULL));
+    CUDA_OK(cudaDeviceSynchronize());
+    MLA_OK_(mla_check_device_error(&bits, 1));
+    if (bits != 0) { fprintf(stderr, "device error bits %d (e4m3)\n", bits); return 4; }
+    CUDA_OK(cudaMemcpy(out8, out_d, (size_t)B * SQ * HQ * DV * 2, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(lse8, lse_d, (size_t)B * HQ * SQ * 4, cudaMemcpyDeviceToHost));
     MLA_OK_(mla_shutdown());
 
     const int64_t qs[3] = {SQ * HQ * D, HQ * D, D}, ks[3] = {P * HK * D, HK * D, D};
@@ -120,6 +166,25 @@ int main(void) {
         if (!(e <= 2e-3)) { fprintf(stderr, "lse %zu: %g vs %g\n", i, lse[i], ref_l[i]); return 7; }
         if (e > max_l) max_l = e;
     }
-    printf("capi ok: parts %d, max |out err| %.3g, max |lse err| %.3g\n", parts, max_o, max_l);
+    /* e4m3: the oracle on the decoded values (exact in bf16) with scale bmm1, output times bmm2 */
+    if (oracle_mla_decode(B, SQ, HQ, HK, D, DV, P, NB, MAXB, q8v, qs, k8v, ks, bt, MAXB, L, (double)bmm1, 1,
+                          NULL, -1, ref_o, ref_l, 1) != 0) {
+        fprintf(stderr, "oracle failed (e4m3)\n");
+        return 5;
+    }
+    double max_o8 = 0.0, max_l8 = 0.0;
+    for (size_t i = 0; i < (size_t)B * SQ * HQ * DV; ++i) {
+        const double r = bmm2 * ref_o[i], e = fabs((double)from_bf16(out8[i]) - r);
+        if (!(e <= 0.03 + 0.03 * fabs(r))) { fprintf(stderr, "e4m3 out %zu: %g vs %g\n", i, from_bf16(out8[i]), r); return 8; }
+        if (e > max_o8) max_o8 = e;
+    }
+    for (size_t i = 0; i < (size_t)B * HQ * SQ; ++i) {
+        if (isinf(ref_l[i]) && isinf(lse8[i]) && lse8[i] < 0) continue;
+        const double e = fabs((double)lse8[i] - ref_l[i]);
+        if (!(e <= 2e-3)) { fprintf(stderr, "e4m3 lse %zu: %g vs %g\n", i, lse8[i], ref_l[i]); return 9; }
+        if (e > max_l8) max_l8 = e;
+    }
+    printf("capi ok: parts %d, max |out err| %.3g, max |lse err| %.3g; e4m3 max |out err| %.3g, |lse err| %.3g\n",
+           parts, max_o, max_l, max_o8, max_l8);
     return 0;
 }

@@ -1,6 +1,6 @@
 """The C ABI driven from a C program (no Python in the call path): schedule,
-decode on the library's own workspace, device error check and shutdown, held
-to the fp64 oracle within the parity bar (tests/c/capi_decode.c)."""
+decode on the library's own workspace (bf16, then the same values in e4m3),
+device error check and shutdown, held to the fp64 oracle (tests/c/capi_decode.c)."""
 import os
 import subprocess
 
@@ -22,4 +22,4 @@ def test_c_program_through_the_c_abi(tmp_path):
                            "-L", os.path.join(CUDA, "lib64"), "-lcudart", "-lm"])
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "capi ok" in r.stdout
+    assert "capi ok" in r.stdout and "e4m3" in r.stdout
