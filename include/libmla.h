@@ -280,12 +280,19 @@ int mla_decode_fwd_split(const mla_shape_t *shape, const mla_rope_strides_t *rop
  *   k_cache  (num_blocks, 64, h_k, 576) e4m3 bytes  strides shape->k_stride
  *   out      (batch, s_q, h_q, 512) bf16, softmax_lse (batch, h_q, s_q) fp32, as mla_decode_fwd
  * Masking, schedule (mla_get_metadata), workspace (NULL = internal) and the
- * two launches are those of mla_decode_fwd.  The probabilities are rounded to
- * e4m3 for the PV product (the denominator sums them unrounded), so the output
- * differs from the exact value by up to 2^-4 of each probability times its
- * value row.  Errors: as mla_decode_fwd, and MLA_ERR_ARG when bmm1_scale is
- * not positive and finite, bmm2_scale not finite, or a q / k_cache stride is
- * not a multiple of 16 bytes.
+ * two launches are those of mla_decode_fwd.
+ *
+ * Accuracy.  The probabilities are rounded to e4m3 for the PV product (the
+ * denominator sums them unrounded): each weight errs by up to 2^-4 of itself.
+ * With more than 32 query rows per KV head the two halves of each logit,
+ * s_0 and s_1 (latent dims 0-255 + RoPE dims 512-543, and the rest), are
+ * rounded to bf16 before they are added, which moves a logit by at most
+ * bmm1_scale * 2^-8 * (|s_0| + |s_1|) and softmax_lse by at most the
+ * probability-weighted mean of those moves.
+ *
+ * Errors: as mla_decode_fwd, and MLA_ERR_ARG when bmm1_scale is not positive
+ * and finite, bmm2_scale not finite, or a q / k_cache stride is not a
+ * multiple of 16 bytes.
  */
 int mla_decode_fwd_fp8(const mla_shape_t *shape, const void *q, const void *k_cache,
                        const int32_t *block_table, const int32_t *cache_seqlens,
