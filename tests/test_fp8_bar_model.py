@@ -1,0 +1,70 @@
+"""The e4m3 parity bar (tests/test_fp8_gpu.py) against a model of the roundings the e4m3
+kernel applies (CPU only).
+
+The model restates the kernel's arithmetic in float64 numpy on the decoded values:
+- logits from the two halves of the dot product, each rounded to bf16 before they are added
+  (the pair's exchange above 32 rows);
+- probabilities 2^(logit * log2(e) - max), rounded to e4m3 for the PV product;
+- the denominator summing the unrounded probabilities.
+Its error against the oracle must stay inside the bar the GPU test applies, with the mean
+well inside, on a diffuse and on a sharp (x8) softmax.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tests.test_fp8_gpu as T
+from oracle import fp8 as F
+from oracle import reference as R
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _e4m3(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("name,sharp,s_q,causal,Ls", [
+    ("diffuse", 1, 1, False, [1, 65, 300]),
+    ("sharp", 8, 1, False, [65, 300]),
+    ("causal", 1, 2, True, [2, 64, 333]),
+])
+def test_rounding_model_stays_inside_the_bar(name, sharp, s_q, causal, Ls):
+    bmm1 = sharp * T.BMM1
+    inp, q8, k8 = T._inputs(name, s_q, 128, Ls, causal=causal, seed=40 + sharp)
+    w = inp.workload
+    B, s_q, h_q, _ = q8.shape
+    rows = list(range(B * s_q * h_q))
+    qv, kv = F.e4m3_decode(q8.numpy()), F.e4m3_decode(k8.numpy())
+    bt, L = inp.block_table.numpy(), inp.cache_seqlens.numpy()
+    h0, h1 = np.r_[0:256, 512:544], np.r_[256:512, 544:576]
+    model_o = np.zeros((len(rows), 512))
+    model_l = np.full(len(rows), -np.inf)
+    for r in rows:
+        b, rem = divmod(r, s_q * h_q)
+        i, h = divmod(rem, h_q)
+        n = R.visible_keys(int(L[b]), s_q, i, causal)
+        if n == 0:
+            continue
+        t = np.arange(n)
+        K = kv[bt[b, t // 64], t % 64, 0]
+        qr = qv[b, i, h]
+        S = _bf16(K[:, h0] @ qr[h0]) + _bf16(K[:, h1] @ qr[h1])
+        lg = S * bmm1 * np.log2(np.e)
+        m = lg.max()
+        p = np.exp2(lg - m)
+        model_o[r] = T.BMM2 * (_e4m3(p)[:, None] * K[:, :512]).sum(axis=0) / p.sum()
+        model_l[r] = (m + np.log2(p.sum())) * np.log(2.0)
+    ref_o, ref_l = F.mla_decode_fp8(q8, k8, inp.block_table, inp.cache_seqlens, bmm1, T.BMM2, causal)
+    ro = ref_o.reshape(-1, 512)
+    rl = ref_l.transpose(0, 2, 1).reshape(-1)
+    sig, out_dl, lse_dl = T._sigma(inp, q8, k8, rows, bmm1)
+    bound = 8 * T.SIGMA_REL * T.BMM2 * sig + 2.0 ** -8 * np.abs(ro) + 2e-3 + out_dl
+    err = np.abs(model_o - ro)
+    assert (err <= bound).all(), f"{name}: max err / bar {(err / bound).max():.3f}"
+    assert err.mean() < 0.25 * bound.mean()
+    ok = np.isfinite(rl)
+    assert (np.abs(model_l[ok] - rl[ok]) <= T.LSE_ATOL + lse_dl[ok]).all()
+    assert np.array_equal(np.isfinite(model_l), ok)
