@@ -223,7 +223,7 @@ int mla_decode_combine(const mla_shape_t *shape, const void *q, const void *k_ca
  * (with a message giving both sizes) when mla_workspace_size(shape) exceeds
  * MLA_NOALLOC_SCRATCH_BYTES.  The first call on a device looks up the
  * scratch's device address with that device current; make it before any
- * stream capture.  All calls share the one scratch array: calls whose
+ * stream capture (and again after mla_shutdown, which forgets it).  All calls share the one scratch array: calls whose
  * kernels may overlap on the GPU (unordered streams) race on it and must not
  * be issued.  Nothing in the scratch needs clearing between calls.
  */
@@ -356,7 +356,12 @@ int mla_decode_fwd_host(const mla_shape_t *shape, const void *q_host, const void
  * Releases the internal workspaces that calls without a workspace allocated
  * and the staging buffers and streams of mla_decode_fwd_host (synchronizing
  * each device that holds one first).  Later such calls
- * allocate again.  Not to be called while another thread uses the library.
+ * allocate again.  It also forgets what the library set up per device
+ * (kernel attributes, the device addresses of its error word and of the
+ * built-in scratch of mla_decode_fwd_noalloc, cache tensor maps), which the
+ * next call on each device sets up again: call it before resetting a device
+ * (cudaDeviceReset), since the reset may reload the library's module at
+ * other addresses.  Not to be called while another thread uses the library.
  * Errors: MLA_ERR_CUDA.
  */
 int mla_shutdown(void);

@@ -42,16 +42,16 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB, build_dir: str = BUILD) -> str:
+    if not force and lib == LIB and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "--expt-relaxed-constexpr", "-Xptxas", "-v"] + list(extra_flags)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     objs, logs, failed = [], [], []
@@ -61,19 +61,27 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         if pr.returncode != 0:
             failed.append(src)
         objs.append(obj)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         f.write("\n".join(logs))
     if failed:
         raise RuntimeError("nvcc failed for " + ", ".join(failed) + "\n" + "\n".join(logs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
         print("\n".join(logs), file=sys.stderr)
-    return LIB
+    return lib
+
+
+def build_variant(name: str, defines) -> str:
+    """A separate copy of the library built with extra preprocessor definitions, under
+    _build/variant_<name>/ (never the package's libmla.so).  The tests use it to build the
+    library with a short limit on the decode kernels' waits."""
+    d = os.path.join(BUILD, "variant_" + name)
+    return build(force=True, extra_flags=[f"-D{x}" for x in defines], lib=os.path.join(d, "libmla.so"), build_dir=d)
 
 
 if __name__ == "__main__":

@@ -26,6 +26,7 @@ uint32_t splitkv_f8_smem_bytes();
 uint32_t splitkv_threads();
 uint32_t combine_threads();
 uint32_t combine_rows_per_block();
+void noalloc_forget_devices();
 }  // namespace mla
 
 // Error bits raised by the kernels on this device (MLA_DEVERR_*).
@@ -838,6 +839,15 @@ int mla_shutdown(void) {
         h = HostEntry();
     }
     cudaSetDevice(prev);
+    {
+        // what was looked up per device (kernel attributes, symbol addresses,
+        // tensor maps) is set up again by the next call: after a context reset
+        // the module may be loaded at other addresses
+        std::lock_guard<std::mutex> dlock(g_mu);
+        for (auto &d : g_dev) d = DeviceState();
+        for (auto &m : g_maps) m.valid = false;
+    }
+    mla::noalloc_forget_devices();
     return status;
 }
 

@@ -411,13 +411,9 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
-#if MLA_F8
-    // bf16 partial logits when more than 32 rows are exchanged (the DSMEM link then bounds the
-    // page rate); one warp's rows stay fp32 (there the softmax's conversions would cost more)
-    const bool xbf16 = p.rows - rb * kRowsPerBlock > 32;
-#else
+    // the partial logits cross between the pair in fp32 for both input types: rounding them
+    // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
     constexpr bool xbf16 = false;
-#endif
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
@@ -533,13 +529,9 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const int row_g = rb * kRowsPerBlock + r;  // row within the KV head's R rows
     const bool row_real = row_g < p.rows;
     const bool warp_active = rb * kRowsPerBlock + warp * 32 < p.rows;
-#if MLA_F8
-    // bf16 partial logits when more than 32 rows are exchanged (the DSMEM link then bounds the
-    // page rate); one warp's rows stay fp32 (there the softmax's conversions would cost more)
-    const bool xbf16 = p.rows - rb * kRowsPerBlock > 32;
-#else
+    // the partial logits cross between the pair in fp32 for both input types: rounding them
+    // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
     constexpr bool xbf16 = false;
-#endif
     const int qi = row_g / p.hpk;              // query token i
     const int qh = hk * p.hpk + row_g % p.hpk; // query head h
     const uint32_t peer = (uint32_t)(cta ^ 1);

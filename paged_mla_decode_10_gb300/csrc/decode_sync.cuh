@@ -1,11 +1,12 @@
 // decode_sync.cuh -- bounded mbarrier waits and the page gather check shared
 // by the split-KV decode kernels.
 //
-// Every wait is bounded: after kTimeoutCycles a role sets the CTA's abort
+// Every wait is bounded: after kWaitLimitCycles a role sets the CTA's abort
 // flag and MLA_DEVERR_TIMEOUT in the device error word and returns false, and
 // the other roles of the CTA see the flag and stop too.  Teardown waits
 // (drain_bar) ignore the flag, so copies and MMAs already in flight complete
-// before shared memory and TMEM are released; they are bounded as well.
+// before shared memory and TMEM are released; they are bounded as well
+// (kTimeoutCycles).
 #pragma once
 
 #include <cstdint>
@@ -15,6 +16,15 @@
 
 namespace mla {
 
+// Limit of the waits of the main loops.  A test build sets MLA_WAIT_LIMIT_CYCLES
+// far below a page's latency, so that the first wait runs out and the timeout
+// path (error bit, drain, exit) is exercised; the library is built without it.
+#ifndef MLA_WAIT_LIMIT_CYCLES
+#define MLA_WAIT_LIMIT_CYCLES 4000000000ll
+#endif
+constexpr long long kWaitLimitCycles = MLA_WAIT_LIMIT_CYCLES;
+// Limit of the teardown waits (drains): long in every build, so that each copy
+// and MMA in flight has landed before shared memory and TMEM are released.
 constexpr long long kTimeoutCycles = 4000000000ll;
 
 struct Ctx {
@@ -37,7 +47,7 @@ static __device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
         if (*c.abort_flag) return false;
-        if (clock64() - t0 > kTimeoutCycles) { raise_timeout(c); return false; }
+        if (clock64() - t0 > kWaitLimitCycles) { raise_timeout(c); return false; }
     }
     return true;
 }

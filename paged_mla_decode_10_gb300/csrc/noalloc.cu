@@ -18,6 +18,9 @@
 //     previous call are never read;
 //   * the first call on a device looks up the array's device address (with
 //     that device current); make that first call before any stream capture.
+//     mla_shutdown forgets the address, so that a call after a context reset
+//     (cudaDeviceReset, which may reload the module elsewhere) looks it up
+//     again.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,6 +31,7 @@
 
 namespace mla {
 int report_error(int status, const char *msg);
+void noalloc_forget_devices();
 }
 
 // The scratch itself: file-scope device memory, MLA_NOALLOC_SCRATCH_BYTES per GPU.
@@ -62,6 +66,12 @@ int scratch_address(void **out) {
 }
 
 }  // namespace
+
+// Called by mla_shutdown: the next call on each device looks the address up again.
+void mla::noalloc_forget_devices() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto &p : g_scratch_ptr) p = nullptr;
+}
 
 extern "C" int mla_decode_fwd_noalloc(const mla_shape_t *shape, const void *q, const void *k_cache,
                                       const int32_t *block_table, const int32_t *cache_seqlens,

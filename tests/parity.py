@@ -61,22 +61,3 @@ def assert_close(out_gpu, lse_gpu, ref_out, ref_lse, rows=None, where=""):
         r = int(np.argmax(lerr))
         raise AssertionError(f"{where}: lse mismatch at row {r}: gpu {lf[r]} ref {rl[r]} (max {lerr.max():.3g})")
     return float(err.max()), float(lerr.max())
-
-
-def sample_rows(inp, n_rows, seed=0, must=()):
-    """Row indices (flattened b*s_q*h_q + i*h_q + h) spread over all sequences,
-    always including the sequences with the most blocks."""
-    w = inp.workload
-    B, s_q, h_q = inp.q.shape[:3]
-    rng = np.random.default_rng(seed)
-    L = inp.cache_seqlens.cpu().numpy()
-    longest = list(np.argsort(-L)[:2])
-    bs = list(dict.fromkeys(longest + list(must) + list(rng.integers(0, B, size=n_rows))))
-    rows = []
-    for b in bs:
-        i = int(rng.integers(0, s_q))
-        for h in (0, int(rng.integers(0, h_q)), h_q - 1):
-            rows.append(b * s_q * h_q + i * h_q + h)
-        if len(rows) >= n_rows:
-            break
-    return sorted(set(rows))
