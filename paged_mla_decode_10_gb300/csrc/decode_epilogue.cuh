@@ -3,10 +3,12 @@
 // After the last PV of a segment, thread r of softmax warp w holds query row
 // 32 w + r of the 128-row block in TMEM lane 32 w + r.  Stored straight from
 // registers, each store instruction of a warp would touch 32 rows with 16
-// bytes apiece.  Here each warp passes its rows through a 32 x 80-byte staging
-// tile in shared memory, so that a store instruction writes eight 64-byte row
-// segments (whole 32-byte sectors): bf16 to `out` when the sequence was not
-// split, fp32 partial rows to the workspace otherwise.
+// bytes apiece.  Here each warp passes its rows through a 32 x 64-byte staging
+// tile in shared memory (16-byte chunks XOR-swizzled by row bits 1-2, so neither
+// the row-wise writes nor the segment-wise reads conflict on banks), so that a
+// store instruction writes eight 64-byte row segments (whole 32-byte sectors):
+// bf16 to `out` when the sequence was not split, fp32 partial rows to the
+// workspace otherwise.
 #pragma once
 
 #include <cstdint>
@@ -16,8 +18,13 @@
 
 namespace mla {
 
-constexpr uint32_t kEpiPitch = 80;                    // bytes per staged row (64 data + 16 pad)
+constexpr uint32_t kEpiPitch = 64;                    // bytes per staged row
 constexpr uint32_t kEpiWarpBytes = 32 * kEpiPitch;    // staging tile of one warp
+
+// Byte offset of 16-byte chunk c of staged row r.
+static __device__ __forceinline__ uint32_t epi_offset(uint32_t r, uint32_t c) {
+    return r * kEpiPitch + ((c ^ ((r >> 1) & 3u)) << 4);
+}
 
 // tmem_o: TMEM address of the warp's lane quadrant at the O columns.
 // stage:  the warp's staging tile (16-byte aligned, kEpiWarpBytes).
@@ -26,7 +33,6 @@ constexpr uint32_t kEpiWarpBytes = 32 * kEpiPitch;    // staging tile of one war
 static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint32_t tmem_o, uint8_t *stage, int lane,
                                                     int row0, int b, int hk, int cta, bool direct, bool slot_ok,
                                                     int slot, float inv) {
-    uint8_t *mine = stage + lane * kEpiPitch;
 #pragma unroll 1
     for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t o[64];
@@ -44,7 +50,7 @@ static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint3
                     w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
                     w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
                     w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-                    reinterpret_cast<uint4 *>(mine)[v] = w;
+                    *reinterpret_cast<uint4 *>(stage + epi_offset(lane, v)) = w;
                 }
                 __syncwarp();
 #pragma unroll
@@ -55,7 +61,7 @@ static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint3
                         const int qi = row_g / p.hpk, qh = hk * p.hpk + row_g % p.hpk;
                         uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)b * p.o_s0 + (int64_t)qi * p.o_s1 +
                                                                (int64_t)qh * p.o_s2 + 256 * cta + 64 * q4 + 32 * sub) + cc;
-                        *dst = *reinterpret_cast<const uint4 *>(stage + rr * kEpiPitch + cc * 16);
+                        *dst = *reinterpret_cast<const uint4 *>(stage + epi_offset(rr, cc));
                     }
                 }
                 __syncwarp();
@@ -67,7 +73,7 @@ static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint3
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int j = 16 * sub + 4 * v;
-                    reinterpret_cast<float4 *>(mine)[v] =
+                    *reinterpret_cast<float4 *>(stage + epi_offset(lane, v)) =
                         make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
                                     __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
                 }
@@ -79,7 +85,7 @@ static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint3
                     if (row_g < p.rows) {
                         const int64_t prow = ((int64_t)slot * p.h_k + hk) * p.rows + row_g;
                         float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * kDv + 256 * cta + 64 * q4 + 16 * sub) + cc;
-                        *dst = *reinterpret_cast<const float4 *>(stage + rr * kEpiPitch + cc * 16);
+                        *dst = *reinterpret_cast<const float4 *>(stage + epi_offset(rr, cc));
                     }
                 }
                 __syncwarp();

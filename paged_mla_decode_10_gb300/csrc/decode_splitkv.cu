@@ -24,9 +24,10 @@
 //
 // Per CTA:
 //   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
-//   smem  Q RoPE half (SW64) | 3-stage page ring (4 x SW128 + 1 x SW64 boxes,
-//         36,864 B per page half) | S exchange: two landing slots and one
-//         staging tile (fp32) | epilogue staging | mbarriers
+//   smem  Q RoPE half (SW64) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
+//         36,864 B per page half) | S exchange: one landing slot and one
+//         staging tile (fp32; each warp's 8 KB of the slot is refilled as soon
+//         as the softmax warp has read it) | epilogue staging | mbarriers
 //   P (bf16) is written back over the S buffer it came from and read by the
 //   PV MMA straight from TMEM.
 //   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
@@ -40,11 +41,10 @@
 // bmm1_scale / bmm2_scale note):
 //   - the MMAs are kind::f8f6f4 (K = 32): 9 per page for QK^T, 2 for PV;
 //   - a page half is 18,432 B (two 128-dim SW128 boxes and one 32-byte SW32
-//     RoPE box), so the ring has six stages;
+//     RoPE box), so the ring has eight stages;
 //   - Q fills TMEM columns [384,448) (e4m3 quads), which leaves [448,512) for
 //     a third S/P buffer: QK^T runs two pages ahead of PV;
-//   - with more than 32 rows the pair exchanges its partial logits as bf16
-//     and both CTAs add bf16(S_0) + bf16(S_1) (half the DSMEM bytes);
+//   - the partial logits cross the pair in fp32, as in bf16;
 //   - P is rounded to e4m3 (quads, 16 columns) for the PV MMA while the
 //     denominator sums the fp32 values, and the epilogue multiplies by
 //     bmm2_scale.
@@ -72,12 +72,16 @@ namespace {
 #ifndef MLA_F8
 #define MLA_F8 0
 #endif
+// One landing slot for the peer's partial tile: a warp's 8 KB of it is refilled as
+// soon as the softmax warp has read it (XINFREE), which leaves room for a deeper
+// page ring.
+constexpr int kXSlots = 1;
 #if MLA_F8
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kLatBoxes = 2;                    // 128 e4m3 dims (128 B rows) per latent box
 constexpr uint32_t kRopeRow = 32;               // bytes per RoPE row: 32 e4m3 dims, SW32
 #else
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kLatBoxes = 4;                    // 64 bf16 dims (128 B rows) per latent box
 constexpr uint32_t kRopeRow = 64;               // bytes per RoPE row: 32 bf16 dims, SW64
 #endif
@@ -86,8 +90,8 @@ constexpr uint32_t kHalfBytes = kRopeOff + 64u * kRopeRow;    // one CTA's 288-d
 constexpr uint32_t kXBytes = 32768;             // one 128 x 64 fp32 partial-logit tile
 constexpr uint32_t OFF_QR = 0;                  // Q RoPE half: 128 rows x kRopeRow
 constexpr uint32_t OFF_K = 128u * kRopeRow;
-constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (2 slots)
-constexpr uint32_t OFF_XOUT = OFF_XIN + 2 * kXBytes;          // our partial tile, staged for the DMA
+constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (kXSlots)
+constexpr uint32_t OFF_XOUT = OFF_XIN + kXSlots * kXBytes;    // our partial tile, staged for the DMA
 constexpr uint32_t OFF_EPI = OFF_XOUT + kXBytes;          // epilogue staging, one tile per softmax warp
 constexpr uint32_t OFF_BAR = OFF_EPI + 4 * kEpiWarpBytes;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
@@ -413,7 +417,6 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
     // the partial logits cross between the pair in fp32 for both input types: rounding them
     // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
-    constexpr bool xbf16 = false;
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
@@ -434,7 +437,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
         for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
             // S/P buffer sb (phase phS); landing slot b of the peer (phase ph)
             const uint32_t sb = it % kSBufs, phS = (it / kSBufs) & 1u;
-            const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
+            const uint32_t b = it % kXSlots, ph = (it / kXSlots) & 1u;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
             if (!ok) break;
             if (!active) {
@@ -450,36 +453,6 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
             if (!ok) break;
-#if MLA_F8
-            if (xbf16) {
-                // the partial logits rounded to bf16 (both CTAs then add bf16(S_0) + bf16(S_1),
-                // bitwise the same sum): 64 B per row and key half, [half][32 rows][64 B],
-                // 16-byte chunks swizzled by (row >> 1) & 3; keys 0-31 leave first
-                uint32_t wb[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) wb[j] = pack_bf16x2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1]));
-                uint8_t *mine = half0 - lane * 128 + lane * 64;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4 *>(mine + ((ch ^ ((lane >> 1) & 3)) << 4)) =
-                        make_uint4(wb[4 * ch], wb[4 * ch + 1], wb[4 * ch + 2], wb[4 * ch + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
-                if (!ok) break;
-                const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
-                const uint32_t src = c.base + OFF_XOUT + (uint32_t)q * 8192u, dst = xin_peer + b * kXBytes;
-                if (lane == 0) bulk_copy_to_peer(dst, src, 2048u, xfull);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4 *>(mine + 2048 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
-                        make_uint4(wb[16 + 4 * ch], wb[16 + 4 * ch + 1], wb[16 + 4 * ch + 2], wb[16 + 4 * ch + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) bulk_copy_to_peer(dst + 2048u, src + 2048u, 2048u, xfull);
-                continue;
-            }
-#endif
             // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
@@ -529,9 +502,6 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const int row_g = rb * kRowsPerBlock + r;  // row within the KV head's R rows
     const bool row_real = row_g < p.rows;
     const bool warp_active = rb * kRowsPerBlock + warp * 32 < p.rows;
-    // the partial logits cross between the pair in fp32 for both input types: rounding them
-    // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
-    constexpr bool xbf16 = false;
     const int qi = row_g / p.hpk;              // query token i
     const int qh = hk * p.hpk + row_g % p.hpk; // query head h
     const uint32_t peer = (uint32_t)(cta ^ 1);
@@ -558,7 +528,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
         for (int blk = s.lo; blk < s.hi && ok; ++blk, ++it) {
             // S/P buffer sb (phase phS); landing slot xb of the peer's tile (phase ph)
             const uint32_t sb = it % kSBufs, phS = (it / kSBufs) & 1u;
-            const uint32_t xb = it & 1u, ph = (it >> 1) & 1u;
+            const uint32_t xb = it % kXSlots, ph = (it / kXSlots) & 1u;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
             if (!ok) break;
             tc_fence_after();
@@ -583,29 +553,11 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             }
             // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
             // add, then tell the peer its staging buffer (and our XIN slot) is free
-            // the peer's partial logits of the warp's 32 rows: 8 KB of fp32, or 4 KB of bf16
-            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), xbf16 ? 4096u : 8192u);
+            // the peer's partial logits of the warp's 32 rows: 8 KB of fp32
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), 8192u);
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + xb), ph));
             if (!ok) break;
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
-#if MLA_F8
-            if (xbf16) {
-                const uint8_t *xrow = smem_gen + OFF_XIN + xb * kXBytes + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 64u;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {   // keys 8ch .. 8ch + 7
-                    const uint4 t = *reinterpret_cast<const uint4 *>(xrow + (ch >> 2) * 2048 +
-                                                                     (((ch & 3) ^ ((r >> 1) & 3)) << 4));
-                    const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int j = 8 * ch + 2 * k;
-                        const uint32_t own = pack_bf16x2(sv[j], sv[j + 1]);
-                        sv[j] = bf16lo_to_f32(own) + bf16lo_to_f32(tw[k]);
-                        sv[j + 1] = bf16hi_to_f32(own) + bf16hi_to_f32(tw[k]);
-                    }
-                }
-            } else
-#endif
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
