@@ -15,9 +15,11 @@
 
 namespace mla {
 __global__ void mla_splitkv_kernel(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
+                                   const __grid_constant__ CUtensorMap kq, const __grid_constant__ CUtensorMap kqr,
                                    const __grid_constant__ DecodeParams p);
 __global__ void mla_splitkv_kernel_f8(const __grid_constant__ CUtensorMap km128,
-                                      const __grid_constant__ CUtensorMap km64, const __grid_constant__ DecodeParams p);
+                                      const __grid_constant__ CUtensorMap km64, const __grid_constant__ CUtensorMap kq,
+                                      const __grid_constant__ CUtensorMap kqr, const __grid_constant__ DecodeParams p);
 __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
 __global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
 size_t metadata_smem_bytes(int batch, int parts);
@@ -389,14 +391,111 @@ int prepare(const mla_shape_t *sh, const void *q, const void *k_cache, const int
     return MLA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// TMA descriptors over the query, so that the decode kernel can bring a
+// segment's Q through its page ring: {dims, h_q, s_q, batch} maps of the
+// latent and of the RoPE dims.  A latent box covers one 128-row block of a KV
+// head (q_hb heads x q_tb tokens), a RoPE box 64 rows.  This needs the blocks
+// to align with heads and tokens (heads per KV head a multiple or a divisor
+// of 128); otherwise, or when the driver rejects a map, the kernel loads Q
+// itself (q_tma = 0).  Cached per (device, query geometry).
+// ---------------------------------------------------------------------------
+struct QMapKey {
+    int device = -1, elem = 0, h_q = 0, s_q = 0, batch = 0, hpk = 0, lat_dims = 0, rope_dims = 0;
+    const void *lat = nullptr, *rope = nullptr;
+    int64_t lat_stride[3] = {0, 0, 0}, rope_stride[3] = {0, 0, 0};
+    bool operator==(const QMapKey &o) const {
+        return device == o.device && elem == o.elem && h_q == o.h_q && s_q == o.s_q && batch == o.batch &&
+               hpk == o.hpk && lat_dims == o.lat_dims && rope_dims == o.rope_dims && lat == o.lat && rope == o.rope &&
+               !memcmp(lat_stride, o.lat_stride, sizeof lat_stride) && !memcmp(rope_stride, o.rope_stride, sizeof rope_stride);
+    }
+};
+struct QMapEntry {
+    QMapKey key;
+    CUtensorMap lat, rope;
+    bool ok = false, valid = false;
+};
+QMapEntry g_qmaps[kMapCache];
+int g_qmap_next = 0;
+
+// Fills the query maps and the q_* fields of p; false (p.q_tma = 0) when Q cannot come by TMA.
+bool query_maps(const mla_shape_t *sh, int elem, DecodeParams &p, CUtensorMap *lat, CUtensorMap *rope) {
+    p.q_tma = 0;
+    const int hpk = p.hpk;
+    if (!(hpk % kRowsPerBlock == 0 || kRowsPerBlock % hpk == 0) || sh->batch < 1) return false;
+    QMapKey k;
+    cudaGetDevice(&k.device);
+    k.elem = elem;
+    k.h_q = sh->h_q; k.s_q = sh->s_q; k.batch = sh->batch; k.hpk = hpk;
+    const bool concat = elem == 1 || p.q_concat;
+    k.lat = elem == 1 ? static_cast<const void *>(p.q8) : static_cast<const void *>(p.q);
+    // a concatenated query has one map base for both: the RoPE boxes start at dim qr_x0 = 512
+    k.rope = concat ? k.lat : static_cast<const void *>(p.q_rope);
+    k.lat_dims = concat ? MLA_HEAD_DIM : MLA_HEAD_DIM_V;
+    k.rope_dims = concat ? MLA_HEAD_DIM : MLA_HEAD_DIM - MLA_HEAD_DIM_V;
+    const int64_t ls[3] = {p.q_s2, p.q_s1, p.q_s0}, rs[3] = {p.qr_s2, p.qr_s1, p.qr_s0};
+    for (int i = 0; i < 3; ++i) {
+        k.lat_stride[i] = ls[i];
+        k.rope_stride[i] = concat ? ls[i] : rs[i];
+    }
+    const int hb = hpk >= kRowsPerBlock ? kRowsPerBlock : hpk, tb = kRowsPerBlock / hb;
+    const int hbr = hpk >= 64 ? 64 : hpk, tbr = 64 / hbr;
+    p.q_hb = hb;
+    p.q_tb = tb;
+    p.qr_x0 = concat ? MLA_HEAD_DIM_V : 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto &e : g_qmaps) {
+        if (e.valid && e.key == k) {
+            *lat = e.lat;
+            *rope = e.rope;
+            p.q_tma = e.ok ? 1 : 0;
+            return e.ok;
+        }
+    }
+    EncodeTiledFn enc;
+    if (get_encoder(&enc) != MLA_OK) return false;
+    const cuuint64_t eb = (cuuint64_t)elem;
+    const cuuint64_t gdim_l[4] = {(cuuint64_t)k.lat_dims, (cuuint64_t)sh->h_q, (cuuint64_t)sh->s_q, (cuuint64_t)sh->batch};
+    const cuuint64_t gdim_r[4] = {(cuuint64_t)k.rope_dims, (cuuint64_t)sh->h_q, (cuuint64_t)sh->s_q, (cuuint64_t)sh->batch};
+    const cuuint64_t gstr_l[3] = {(cuuint64_t)k.lat_stride[0] * eb, (cuuint64_t)k.lat_stride[1] * eb,
+                                  (cuuint64_t)k.lat_stride[2] * eb};
+    const cuuint64_t gstr_r[3] = {(cuuint64_t)k.rope_stride[0] * eb, (cuuint64_t)k.rope_stride[1] * eb,
+                                  (cuuint64_t)k.rope_stride[2] * eb};
+    // latent boxes of 128-byte rows (SW128); RoPE boxes of 32 dims: 64-byte rows (SW64) in bf16,
+    // 32-byte rows (SW32) in e4m3 -- the layouts of the Q RoPE tile the kernel keeps
+    const cuuint32_t box_l[4] = {(cuuint32_t)(128 / elem), (cuuint32_t)hb, (cuuint32_t)tb, 1},
+                     box_r[4] = {32, (cuuint32_t)hbr, (cuuint32_t)tbr, 1}, es[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle rsw = elem == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    QMapEntry &e = g_qmaps[g_qmap_next];
+    g_qmap_next = (g_qmap_next + 1) % kMapCache;
+    e.key = k;
+    CUresult r1 = enc(&e.lat, dt, 4, const_cast<void *>(k.lat), gdim_l, gstr_l, box_l, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r2 = enc(&e.rope, dt, 4, const_cast<void *>(k.rope), gdim_r, gstr_r, box_r, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, rsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    e.ok = r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS;
+    e.valid = true;
+    *lat = e.lat;
+    *rope = e.rope;
+    p.q_tma = e.ok ? 1 : 0;
+    return e.ok;
+}
+
 int launch_splitkv(const mla_shape_t *sh, const KvSource &src, const Prepared &pr, cudaStream_t stream) {
-    CUtensorMap m128, m64;
+    CUtensorMap m128, m64, mq, mqr;
     int st = kcache_maps(sh, src, &m128, &m64);
     if (st != MLA_OK) return st;
+    DecodeParams p = pr.p;
+    if (!query_maps(sh, src.elem, p, &mq, &mqr)) {
+        memset(&mq, 0, sizeof mq);
+        memset(&mqr, 0, sizeof mqr);
+    }
     if (src.elem == 1)
-        mla_splitkv_kernel_f8<<<pr.grid, splitkv_threads(), splitkv_f8_smem_bytes(), stream>>>(m128, m64, pr.p);
+        mla_splitkv_kernel_f8<<<pr.grid, splitkv_threads(), splitkv_f8_smem_bytes(), stream>>>(m128, m64, mq, mqr, p);
     else
-        mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, pr.p);
+        mla_splitkv_kernel<<<pr.grid, splitkv_threads(), splitkv_smem_bytes(), stream>>>(m128, m64, mq, mqr, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
     return MLA_OK;
@@ -846,6 +945,7 @@ int mla_shutdown(void) {
         std::lock_guard<std::mutex> dlock(g_mu);
         for (auto &d : g_dev) d = DeviceState();
         for (auto &m : g_maps) m.valid = false;
+        for (auto &m : g_qmaps) m.valid = false;
     }
     mla::noalloc_forget_devices();
     return status;

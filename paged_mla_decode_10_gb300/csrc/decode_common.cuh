@@ -40,6 +40,11 @@ struct DecodeParams {
     float scale_log2;              // softmax_scale * log2(e) (bmm1_scale * log2(e) for e4m3 inputs)
     const uint8_t *q8;             // e4m3 q (B, s_q, h_q, 576), strides q_s0..2 in bytes (e4m3 kernel only)
     float out_scale;               // bmm2_scale: factor on the output of the e4m3 kernel
+    // Q by TMA (q_tma = 1): the tensor maps of the latent and RoPE query dims
+    // {dims, h_q, s_q, batch}; a latent box covers a 128-row block (q_hb heads x
+    // q_tb tokens), a RoPE box 64 rows; the RoPE boxes start at dim qr_x0.
+    int q_tma;
+    int q_hb, q_tb, qr_x0;
 };
 
 // One contiguous run of blocks of one sequence assigned to a part.

@@ -17,22 +17,32 @@
 // CTA therefore streams a disjoint 288-dim half of every page from HBM (no
 // byte is read twice), computes a partial logit tile S_c = Q_c K_c^T on the
 // tensor core, and the two CTAs swap their partial tiles through distributed
-// shared memory.  S = S_0 + S_1 is then bitwise identical in both CTAs, both
-// run the same online softmax, and each accumulates its half of
-// O = softmax(S) V.  The fp32 O half (128 x 256) fills half of TMEM, which
-// leaves room for two logit buffers and the resident Q half.
+// shared memory.  Each CTA adds the peer's tile to its own, runs the online
+// softmax on S = S_0 + S_1 and accumulates its half of O = softmax(S) V.  The
+// fp32 O half (128 x 256) fills half of TMEM, which leaves room for two logit
+// buffers and the resident Q half.
+//
+// Exchange format.  A tile crosses the pair as 16-bit integers with one scale
+// per row and page (block floating point): the 64 partial logits x_j of a row
+// are sent as round(x_j 2^(14-E) (1 - 2^-16)) with E the exponent of their
+// largest magnitude, so the receiver adds each x_j to within 2^-15 of that
+// magnitude.  Half the bytes of fp32 cross the link, which bounds the page
+// period.  The lse then moves by at most about 2^-15 times the largest scaled
+// partial logit of a row (1e-5 for logits of order 1, 2e-3 at 65), while the
+// own half stays exact.  MLA_XEXACT = 1 builds the fp32 exchange instead.
 //
 // Per CTA:
 //   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
 //   smem  Q RoPE half (SW64) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
-//         36,864 B per page half) | S exchange: one landing slot and one
-//         staging tile (fp32; each warp's 8 KB of the slot is refilled as soon
-//         as the softmax warp has read it) | epilogue staging | mbarriers
+//         36,864 B per page half) | S exchange: landing slot(s) and staging
+//         tile(s), 16,896 B each (a warp's 4,224 B of a slot are refilled as
+//         soon as the softmax warp has read them) | epilogue staging | mbarriers
 //   P (bf16) is written back over the S buffer it came from and read by the
 //   PV MMA straight from TMEM.
 //   warps 0-3  softmax / epilogue, thread r = query row r (= TMEM lane r)
 //   warps 4-7  logit exchange: S out of TMEM, staged, DMA'd to the peer
-//   warp  8    TMA producer: page gather through block_table, Q prefetch
+//   warp  8    TMA producer: a segment's Q, then its pages (block_table
+//              gather), through the same ring
 //   warp  9    MMA issuer (one lane) + TMEM allocation
 //
 // e4m3 variant.  The same source compiled with MLA_F8=1 (decode_splitkv_fp8.cu)
@@ -44,7 +54,9 @@
 //     RoPE box), so the ring has eight stages;
 //   - Q fills TMEM columns [384,448) (e4m3 quads), which leaves [448,512) for
 //     a third S/P buffer: QK^T runs two pages ahead of PV;
-//   - the partial logits cross the pair in fp32, as in bf16;
+//   - the smaller ring leaves room for two landing slots and two staging
+//     tiles, so a page's partial tile leaves while the previous one is still
+//     crossing or being read;
 //   - P is rounded to e4m3 (quads, 16 columns) for the PV MMA while the
 //     denominator sums the fp32 values, and the epilogue multiplies by
 //     bmm2_scale.
@@ -72,10 +84,30 @@ namespace {
 #ifndef MLA_F8
 #define MLA_F8 0
 #endif
-// One landing slot for the peer's partial tile: a warp's 8 KB of it is refilled as
-// soon as the softmax warp has read it (XINFREE), which leaves room for a deeper
-// page ring.
-constexpr int kXSlots = 1;
+#ifndef MLA_XEXACT
+#define MLA_XEXACT 0
+#endif
+// Landing slots for the peer's partial tiles (a slot is refilled once the softmax
+// warps have read it: XINFREE) and staging tiles for ours (one is rewritten once
+// the peer has received the tile it held: STAGEFREE).  With two of each, the tile
+// of page i leaves while that of page i - 1 is still in flight or being read.
+#ifndef MLA_XIN_SLOTS
+#if MLA_F8 && !MLA_XEXACT
+#define MLA_XIN_SLOTS 2
+#else
+#define MLA_XIN_SLOTS 1   // a second one does not fit beside the page ring
+#endif
+#endif
+#ifndef MLA_XOUT_SLOTS
+#if MLA_F8 && !MLA_XEXACT
+#define MLA_XOUT_SLOTS 2
+#else
+#define MLA_XOUT_SLOTS 1
+#endif
+#endif
+constexpr int kXSlots = MLA_XIN_SLOTS;
+constexpr int kXOut = MLA_XOUT_SLOTS;
+static_assert(kXSlots >= 1 && kXSlots <= 2 && kXOut >= 1 && kXOut <= 2, "exchange buffers");
 #if MLA_F8
 constexpr int kStages = 8;
 constexpr int kLatBoxes = 2;                    // 128 e4m3 dims (128 B rows) per latent box
@@ -87,12 +119,25 @@ constexpr uint32_t kRopeRow = 64;               // bytes per RoPE row: 32 bf16 d
 #endif
 constexpr uint32_t kRopeOff = kLatBoxes * 8192u;              // RoPE box within a stage
 constexpr uint32_t kHalfBytes = kRopeOff + 64u * kRopeRow;    // one CTA's 288-dim half of a page
-constexpr uint32_t kXBytes = 32768;             // one 128 x 64 fp32 partial-logit tile
+// The partial logit tile a warp sends for its 32 rows (64 keys each).
+#if MLA_XEXACT
+constexpr uint32_t kXWarpBytes = 8192;          // fp32: [key half][32 rows][128 B]
+#else
+constexpr uint32_t kXWarpBytes = 32 * 128 + 32 * 4;   // 16-bit codes: [32 rows][128 B], then a scale word per row
+// 16-bit block format of a row's 64 partial logits x_j: E = exponent of max |x_j|,
+// code k_j = round(x_j 2^(14-E) (1 - 2^-16)) + 32768 in [1, 65535]; the receiver adds
+// (k_j - 32768) 2^(E-14) (1 + 2^-16), within 2^(E-15) <= max |x_j| 2^-15 of x_j.
+constexpr float kXMagic = 12615680.0f;          // 1.5 * 2^23 + 2^15: fma(x, s, kXMagic) holds k in its low 16 bits
+constexpr float kXBias = 8421376.0f;            // 2^23 + 2^15: float(0x4B000000 | k) - kXBias = k - 32768
+constexpr float kXTrim = 0.9999847412109375f;   // 1 - 2^-16: keeps |x s| below 32767.5
+constexpr float kXUntrim = 1.0000152587890625f; // 1 + 2^-16 = 1 / (1 - 2^-16) to within 2^-32
+#endif
+constexpr uint32_t kXBytes = 4 * kXWarpBytes;   // one 128 x 64 partial-logit tile
 constexpr uint32_t OFF_QR = 0;                  // Q RoPE half: 128 rows x kRopeRow
 constexpr uint32_t OFF_K = 128u * kRopeRow;
 constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (kXSlots)
-constexpr uint32_t OFF_XOUT = OFF_XIN + kXSlots * kXBytes;    // our partial tile, staged for the DMA
-constexpr uint32_t OFF_EPI = OFF_XOUT + kXBytes;          // epilogue staging, one tile per softmax warp
+constexpr uint32_t OFF_XOUT = OFF_XIN + kXSlots * kXBytes;    // our partial tiles, staged for the DMA (kXOut)
+constexpr uint32_t OFF_EPI = OFF_XOUT + kXOut * kXBytes;  // epilogue staging, one tile per softmax warp
 constexpr uint32_t OFF_BAR = OFF_EPI + 4 * kEpiWarpBytes;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
@@ -109,6 +154,25 @@ constexpr int kSBufs = 2;
 constexpr int kPvBars = 1;
 #endif
 constexpr int kLag = kSBufs - 1;                // PV(i) is issued after QK^T(i + kLag)
+#if MLA_F8
+constexpr int kPvKeys = 32;                     // keys per PV MMA (K step)
+#else
+constexpr int kPvKeys = 16;
+#endif
+constexpr int kPvSteps = kPage / kPvKeys;
+
+// Largest of 64 values by a pairwise tree (depth 6 instead of a 64-long chain).
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+    float t[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) t[i] = fmaxf(v[i], v[i + 32]);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    }
+    return t[0];
+}
 
 // barrier indices
 constexpr int B_KFULL = 0;
@@ -118,8 +182,8 @@ constexpr int B_SREAD = B_SFULL + kSBufs;       // exchange warps have read S ou
 constexpr int B_PFULL = B_SREAD + kSBufs;
 constexpr int B_XFULL = B_PFULL + kSBufs;       // peer's partial tile has landed in XIN
 constexpr int B_XINFREE = B_XFULL + 2;          // peer has read the tile we sent into its XIN slot
-constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received our last tile: XOUT reusable
-constexpr int B_PVDONE = B_STAGEFREE + 1;      // kPvBars of them, page i on PVDONE + i % kPvBars
+constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received the tile of an XOUT buffer: reusable
+constexpr int B_PVDONE = B_STAGEFREE + 2;      // kPvBars of them, page i on PVDONE + i % kPvBars
 constexpr int B_OFINAL = B_PVDONE + kPvBars;
 constexpr int B_QREADY = B_OFINAL + 1;
 constexpr int B_DRAIN = B_QREADY + 1;
@@ -148,16 +212,47 @@ constexpr float kRescaleThreshold = 8.0f;        // log2 units
 // softmax warps' Q loads at the segment switch hit L2.
 // ----------------------------------------------------------------------------
 __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtensorMap *km128,
-                              const CUtensorMap *km64, const int32_t *rec, int cta, int rb, int hk,
-                              uint64_t policy) {
+                              const CUtensorMap *km64, const CUtensorMap *kq, const CUtensorMap *kqr,
+                              const int32_t *rec, int cta, int rb, int hk, uint64_t policy) {
     const int lane = threadIdx.x & 31;
     SegmentWalk walk;
     walk.init(rec);
     Segment s;
-    uint32_t it = 0;
+    uint32_t it = 0;   // ring stages issued (Q stages and pages)
     bool ok = true, first = true;
+    // the block's first row, and the row 64 below it, as (head, token) of the query tensor
+    const int r0 = rb * kRowsPerBlock;
+    const int qh0 = hk * p.hpk + r0 % p.hpk, qt0 = r0 / p.hpk;
+    const int qh1 = hk * p.hpk + (r0 + 64) % p.hpk, qt1 = (r0 + 64) / p.hpk;
     while (ok && walk.next(p, s)) {
-        if (!first) prefetch_q_rows(p, s.b, rb, hk, cta, lane);
+        if (p.q_tma) {
+            // Q of the segment in two ring stages, ahead of its pages: stage A holds latent dims
+            // [0, 128) of this CTA's half (RoPE rows 0-63), stage B dims [128, 256) (rows 64-127)
+            for (int h = 0; h < 2 && ok; ++h) {
+                if (lane == 0) {
+                    const uint32_t st = it % kStages;
+                    ok = wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u);
+                    if (ok) {
+                        const uint32_t full = bar_addr(c, B_KFULL + st);
+                        const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
+                        mbar_arrive_expect_tx(full, kHalfBytes);
+#if MLA_F8
+                        tma_load_4d(dst, kq, full, 256 * cta + 128 * h, qh0, qt0, s.b, policy);
+#else
+                        tma_load_4d(dst, kq, full, 256 * cta + 128 * h, qh0, qt0, s.b, policy);
+                        tma_load_4d(dst + 16384u, kq, full, 256 * cta + 128 * h + 64, qh0, qt0, s.b, policy);
+#endif
+                        tma_load_4d(dst + kRopeOff, kqr, full, p.qr_x0 + 32 * cta, h ? qh1 : qh0, h ? qt1 : qt0,
+                                    s.b, policy);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                ++it;
+            }
+            if (!ok) break;
+        } else if (!first) {
+            prefetch_q_rows(p, s.b, rb, hk, cta, lane);
+        }
         first = false;
         for (int base = s.lo; base < s.hi && ok; base += 32) {
             const int n = s.hi - base < 32 ? s.hi - base : 32;
@@ -197,8 +292,12 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
 // ----------------------------------------------------------------------------
 // MMA issuer.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i, bool first_of_seg, int lane) {
-    const uint32_t st = i % kStages, pb = i % kSBufs;
+// PV of page i (its page half in ring stage si % kStages), over its first
+// nsteps K steps of kPvKeys keys (fewer than kPvSteps on a sequence's last,
+// partly filled page).
+__device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i, uint32_t si, bool first_of_seg,
+                                         int nsteps, int lane) {
+    const uint32_t st = si % kStages, pb = i % kSBufs;
     bool ok = wait_bar(c, bar_addr(c, B_PFULL + pb), (i / kSBufs) & 1u);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return false;
@@ -210,7 +309,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
         const uint64_t bd0 = make_sdesc(c.base + OFF_K + st * kHalfBytes, 8192, 1024, kSwizzle128B);
         const uint32_t pa = tmem + s_col(pb);   // P (e4m3 quads, 8 columns per 32 keys) where its S was
         umma_ts_f8(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
-        umma_ts_f8(tmem + TM_O, pa + 8u, bd0 + 256u, idPV, 1u);   // +32 keys = +4096 B
+        if (nsteps > 1) umma_ts_f8(tmem + TM_O, pa + 8u, bd0 + 256u, idPV, 1u);   // +32 keys = +4096 B
 #else
         constexpr uint32_t idPV = make_idesc_bf16(128, 256, false, true);
         // V of this stage, MN-major: 4 boxes of 64 dims (LBO 8 KB), 8-key groups 1 KB apart
@@ -218,8 +317,8 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
         const uint32_t pa = tmem + s_col(pb);   // P (bf16 pairs, 8 columns per 16 keys) where its S was
         umma_ts(tmem + TM_O, pa, bd0, idPV, first_of_seg ? 0u : 1u);
 #pragma unroll
-        for (int kk = 1; kk < 4; ++kk)   // +16 keys = +2048 B = +128 in the descriptor's 16-byte units
-            umma_ts(tmem + TM_O, pa + 8u * kk, bd0 + 128u * kk, idPV, 1u);
+        for (int kk = 1; kk < kPvSteps; ++kk)   // +16 keys = +2048 B = +128 in the descriptor's 16-byte units
+            if (kk < nsteps) umma_ts(tmem + TM_O, pa + 8u * kk, bd0 + 128u * kk, idPV, 1u);
 #endif
         umma_commit(bar_addr(c, B_KEMPTY + st));
         umma_commit(bar_addr(c, B_PVDONE + i % kPvBars));
@@ -232,7 +331,7 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
     SegmentWalk walk;
     walk.init(rec);
     Segment s;
-    uint32_t it = 0, g = 0;
+    uint32_t it = 0, g = 0, si = 0;   // pages, segments, ring stages (Q stages and pages)
     bool ok = true;
 #if MLA_F8
     constexpr uint32_t idS = make_idesc_e4m3(128, 64, false, false);
@@ -243,25 +342,35 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
         ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_QREADY), g & 1u));
         if (!ok) break;
         tc_fence_after();
+        if (p.q_tma) {
+            // Q is in TMEM / smem: the two ring stages it came through are free again
+            if (lane == 0) {
+                mbar_arrive(bar_addr(c, B_KEMPTY + si % kStages));
+                mbar_arrive(bar_addr(c, B_KEMPTY + (si + 1) % kStages));
+            }
+            si += 2;
+        }
         const int nb_seq = (s.L + kPage - 1) / kPage;
         const int tail = s.L & (kPage - 1);
         const int n = s.hi - s.lo;
-        for (int j = 0; j < n; ++j, ++it) {
-            const uint32_t st = it % kStages, sb = it % kSBufs;
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (it / kStages) & 1u));
+        for (int j = 0; j < n; ++j, ++it, ++si) {
+            const uint32_t st = si % kStages, sb = it % kSBufs;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (si / kStages) & 1u));
             if (!ok) break;
             const uint32_t stage = c.base + OFF_K + st * kHalfBytes;
             if (s.lo + j == nb_seq - 1 && tail != 0) {
-                // Rows past the sequence end may hold anything (even NaN); the
-                // P.V product would turn 0 * NaN into NaN, so zero them here.
+                // Rows past the sequence end may hold anything (even NaN).  Their logits
+                // are masked, and the PV of this page stops after the K step holding the
+                // last real row; that step's rows past the end would turn 0 * NaN into
+                // NaN, so their V dims are zeroed here (whole 128-byte box rows, so the
+                // swizzle does not matter).
                 uint8_t *gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(stage));
-                const int rows = kPage - tail;
-                constexpr int kLatCh = kLatBoxes * 8, kRowCh = kLatCh + (int)kRopeRow / 16;   // 16-byte chunks
-                for (int idx = lane; idx < rows * kRowCh; idx += 32) {
-                    const int r = tail + idx / kRowCh, ch = idx % kRowCh;
-                    uint8_t *dst = ch < kLatCh ? gen + (ch >> 3) * 8192 + r * 128 + (ch & 7) * 16
-                                               : gen + kRopeOff + r * kRopeRow + (ch - kLatCh) * 16;
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                const int rows = (tail + kPvKeys - 1) / kPvKeys * kPvKeys - tail;
+                constexpr int kLatCh = kLatBoxes * 8;   // 16-byte chunks of a row's V dims
+                for (int idx = lane; idx < rows * kLatCh; idx += 32) {
+                    const int r = tail + idx / kLatCh, ch = idx % kLatCh;
+                    *reinterpret_cast<uint4 *>(gen + (ch >> 3) * 8192 + r * 128 + (ch & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -296,14 +405,18 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
             }
             __syncwarp();
             if (j >= kLag) {
-                if (!issue_pv(c, tmem, it - kLag, j == kLag, lane)) { ok = false; break; }
+                const int pg = s.lo + j - kLag;
+                const int nst = (pg == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
+                if (!issue_pv(c, tmem, it - kLag, si - kLag, j == kLag, nst, lane)) { ok = false; break; }
             }
         }
         if (!ok) break;
         // the segment's last kLag pages (page n - d is its first when n == d)
 #pragma unroll
         for (int d = kLag; d >= 1; --d) {
-            if (n >= d && !issue_pv(c, tmem, it - d, n == d, lane)) { ok = false; break; }
+            const int pg = s.hi - d;
+            const int nst = (pg == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
+            if (n >= d && !issue_pv(c, tmem, it - d, si - d, n == d, nst, lane)) { ok = false; break; }
         }
         if (!ok) break;
         if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
@@ -399,6 +512,58 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
 }
 
 // ----------------------------------------------------------------------------
+// Q of a segment from the two ring stages the producer loaded it into by TMA
+// (stage counters si, si + 1): warp 4+q moves rows 32q..32q+31 (TMEM lane
+// quadrant q).  A latent box holds 128 rows of 128 bytes (SW128, the rows in
+// TMEM lane order); its row goes to TMEM in 32-column runs.  A RoPE box holds
+// 64 rows in the Q RoPE tile's own layout, so its rows are copied as they are.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ bool copy_q_stages(const Ctx &c, uint32_t tmem_q, int q, int lane, uint32_t si) {
+    const uint32_t m = (uint32_t)(q * 32 + lane);   // row of the block = TMEM lane
+    bool ok = true;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t sj = si + (uint32_t)h;
+        ok = ok && __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + sj % kStages), (sj / kStages) & 1u));
+    }
+    if (!ok) return false;
+    uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
+    const uint32_t row_in_box = (m >> 3) * 1024u + (m & 7u) * 128u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint8_t *stage = smem_gen + OFF_K + ((si + (uint32_t)h) % kStages) * kHalfBytes;
+#if MLA_F8
+        constexpr int kBoxes = 1;   // 128 e4m3 dims per box
+#else
+        constexpr int kBoxes = 2;   // 64 bf16 dims per box
+#endif
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+            const uint8_t *row = stage + bx * 16384u + row_in_box;
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 t = *reinterpret_cast<const uint4 *>(row + ((j ^ (m & 7u)) << 4));
+                w[4 * j] = t.x; w[4 * j + 1] = t.y; w[4 * j + 2] = t.z; w[4 * j + 3] = t.w;
+            }
+            tmem_st_32x32b_x32(tmem_q + 32u * (uint32_t)(h * kBoxes + bx), w);
+        }
+        // this quadrant's RoPE rows sit in stage A (rows 0-63) or B (rows 64-127)
+        if ((q >> 1) == h) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(stage + kRopeOff + (m & 63u) * kRopeRow);
+            uint4 *dst = reinterpret_cast<uint4 *>(smem_gen + OFF_QR + m * kRopeRow);
+#pragma unroll
+            for (int k = 0; k < (int)kRopeRow / 16; ++k) dst[k] = src[k];
+        }
+    }
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar_addr(c, B_QREADY));
+    return true;
+}
+
+// ----------------------------------------------------------------------------
 // Exchange warps (4-7): ship this CTA's partial logit tile to the peer CTA.
 // Warp 4+q owns TMEM lane quadrant q, thread (4+q, l) row r = 32q + l: it
 // copies its row of S out of TMEM into the staging tile XOUT, and lane 0
@@ -418,11 +583,11 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     // the partial logits cross between the pair in fp32 for both input types: rounding them
     // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
     const uint32_t peer = (uint32_t)(cta ^ 1);
-    const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * 8192u, peer);
+    const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * kXWarpBytes, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
-    // staging layout of a warp's 8 KB: [column half][32 rows][128 B], 16-byte chunks swizzled by row
+    // staging layout of a warp's tile: 128-byte row pieces, 16-byte chunks swizzled by row
     uint8_t *half0 = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT +
-                     (uint32_t)q * 8192u + (uint32_t)lane * 128u;
+                     (uint32_t)q * kXWarpBytes + (uint32_t)lane * 128u;
 
     const uint32_t tmem_q = tmem + lane_base + TM_Q;
 
@@ -430,9 +595,13 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     walk.init(rec);
     Segment s, s_next;
     uint32_t it = 0, g = 0;
+    uint32_t si = 0;   // ring stage of the segment's Q (when Q comes by TMA: two stages, then its pages)
     bool ok = true;
     bool have = walk.next(p, s);
-    if (have) load_q_half(c, p, tmem_q, q, lane, rb, cta, hk, s);
+    if (have) {
+        if (p.q_tma) ok = copy_q_stages(c, tmem_q, q, lane, si);
+        else load_q_half(c, p, tmem_q, q, lane, rb, cta, hk, s);
+    }
     while (ok && have) {
         for (int blk = s.lo; blk < s.hi; ++blk, ++it) {
             // S/P buffer sb (phase phS); landing slot b of the peer (phase ph)
@@ -451,33 +620,80 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE), (it & 1u) ^ 1u));
+            // staging buffer ob (phase oph)
+            const uint32_t ob = it % kXOut, oph = (it / kXOut) & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE + ob), oph ^ 1u));
             if (!ok) break;
+            const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
+            const uint32_t src = c.base + OFF_XOUT + ob * kXBytes + (uint32_t)q * kXWarpBytes, dst = xin_peer + b * kXBytes;
+            uint8_t *const stg = half0 + ob * kXBytes;   // this lane's row in buffer ob
+#if MLA_XEXACT
             // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(half0 + ((ch ^ (lane & 7)) << 4)) =
+                *reinterpret_cast<uint4 *>(stg + ((ch ^ (lane & 7)) << 4)) =
                     make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
             if (!ok) break;
-            const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
-            const uint32_t src = c.base + OFF_XOUT + (uint32_t)q * 8192u, dst = xin_peer + b * kXBytes;
             if (lane == 0) bulk_copy_to_peer(dst, src, 4096u, xfull);
 #pragma unroll
             for (int ch = 8; ch < 16; ++ch)
-                *reinterpret_cast<uint4 *>(half0 + 4096 + (((ch - 8) ^ (lane & 7)) << 4)) =
+                *reinterpret_cast<uint4 *>(stg + 4096 + (((ch - 8) ^ (lane & 7)) << 4)) =
                     make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) bulk_copy_to_peer(dst + 4096u, src + 4096u, 4096u, xfull);
+#else
+            {
+                // the row in the 16-bit block format: one scale exponent, 64 codes.  Keys
+                // past the sequence end (rows of a partly filled last page may hold
+                // anything) are sent as 0, so that they cannot set the scale.
+                const int past = s.L - blk * kPage;
+                if (past < kPage) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) raw[j] = j < past ? raw[j] : 0u;
+                }
+                float av[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) av[j] = fabsf(__uint_as_float(raw[j]));
+                const float amax = max64(av);
+                uint32_t eb = (__float_as_uint(amax) >> 23) & 255u;   // biased exponent E + 127
+                eb = eb < 15u ? 15u : (eb > 254u ? 254u : eb);
+                const float sc = __uint_as_float((268u - eb) << 23) * kXTrim;   // 2^(14-E) (1 - 2^-16)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 8 * ch + 2 * e;
+                        const float t0 = fmaf(__uint_as_float(raw[j]), sc, kXMagic);
+                        const float t1 = fmaf(__uint_as_float(raw[j + 1]), sc, kXMagic);
+                        w4[e] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+                    }
+                    *reinterpret_cast<uint4 *>(stg + ((ch ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                *reinterpret_cast<uint32_t *>(stg - lane * 128u + 4096u + lane * 4u) = eb;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+            if (!ok) break;
+            if (lane == 0) bulk_copy_to_peer(dst, src, kXWarpBytes, xfull);
+#endif
         }
         if (!ok) break;
-        // Q of the next segment, once every MMA of this one has completed; the
-        // softmax warps store this segment's output meanwhile
+        // Q of the next segment; the softmax warps store this segment's output meanwhile
         const bool have_next = walk.next(p, s_next);
-        if (have_next) {
+        if (have_next && p.q_tma) {
+            // already in the ring (the producer runs ahead); its TMEM columns and RoPE tile
+            // are free, since this segment's last QK^T completed (its S was read above)
+            si += 2u + (uint32_t)(s.hi - s.lo);
+            ok = copy_q_stages(c, tmem_q, q, lane, si);
+            if (!ok) break;
+        } else if (have_next) {
+            // loaded by this warp, once every MMA of this segment has completed
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_OFINAL), g & 1u));
             if (!ok) break;
             tc_fence_after();
@@ -488,7 +704,10 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
         ++g;
     }
     // Drain: the last tile sent must have landed before the CTAs may exit.
-    if (active && it > 0u) drain_bar(c, bar_addr(c, B_STAGEFREE), (it - 1u) & 1u);
+    if (active) {
+        for (uint32_t j = it > (uint32_t)kXOut ? it - kXOut : 0u; j < it; ++j)
+            drain_bar(c, bar_addr(c, B_STAGEFREE + j % kXOut), (j / kXOut) & 1u);
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -508,11 +727,12 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 
     // shared addresses
     // this row in the landing slots: warp block of 8 KB = [column half][32 rows][128 B]
-    const uint32_t xrow_local[2] = {c.base + OFF_XIN + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 128u,
-                                    c.base + OFF_XIN + kXBytes + (uint32_t)warp * 8192u + (uint32_t)(r & 31) * 128u};
+    const uint32_t xrow_local[2] = {c.base + OFF_XIN + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u,
+                                    c.base + OFF_XIN + kXBytes + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u};
     const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE), peer),
                                     mapa_shared(bar_addr(c, B_XINFREE + 1), peer)};
-    const uint32_t stagefree_peer = mapa_shared(bar_addr(c, B_STAGEFREE), peer);
+    const uint32_t stagefree_peer[2] = {mapa_shared(bar_addr(c, B_STAGEFREE), peer),
+                                        mapa_shared(bar_addr(c, B_STAGEFREE + 1), peer)};
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 
     SegmentWalk walk;
@@ -551,13 +771,15 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
             }
-            // ---- the peer's partial logits: arm XFULL for this warp's 8 KB, wait,
-            // add, then tell the peer its staging buffer (and our XIN slot) is free
-            // the peer's partial logits of the warp's 32 rows: 8 KB of fp32
-            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), 8192u);
+            // ---- the peer's partial logits of the warp's 32 rows: arm XFULL for the
+            // warp's tile, wait, add, then tell the peer its staging buffer (and our XIN
+            // slot) is free
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), kXWarpBytes);
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + xb), ph));
             if (!ok) break;
-            if ((r & 31) == 0) mbar_arrive_remote_relaxed(stagefree_peer);   // the peer's DMA has landed
+            if ((r & 31) == 0)   // the peer's DMA has landed: its staging buffer it % kXOut is free
+                mbar_arrive_remote_relaxed(it % kXOut ? stagefree_peer[1] : stagefree_peer[0]);
+#if MLA_XEXACT
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
@@ -565,6 +787,24 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                     (((ch & 7) ^ (r & 7)) << 4));
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
+#else
+            {
+                const uint8_t *xr = smem_gen + ((xb ? xrow_local[1] : xrow_local[0]) - c.base);
+                const uint32_t eb = *reinterpret_cast<const uint32_t *>(xr - (r & 31) * 128 + 4096 + (r & 31) * 4);
+                const float inv = __uint_as_float((eb - 14u) << 23) * kXUntrim;   // 2^(E-14) (1 + 2^-16)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 t = *reinterpret_cast<const uint4 *>(xr + ((ch ^ (r & 7)) << 4));
+                    const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 8 * ch + 2 * e;
+                        sv[j] = fmaf(__uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5410)) - kXBias, inv, sv[j]);
+                        sv[j + 1] = fmaf(__uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5432)) - kXBias, inv, sv[j + 1]);
+                    }
+                }
+            }
+#endif
             __syncwarp();
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(xb ? xfree_peer[1] : xfree_peer[0]);
 
@@ -575,9 +815,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sv[j] = j < nv ? sv[j] : -INFINITY;
             }
-            float mraw = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) mraw = fmaxf(mraw, sv[j]);
+            const float mraw = max64(sv);
             const float mt = mraw * p.scale_log2;   // -inf stays -inf
             const bool o_live = m_ref != -INFINITY;
             const bool raise = mt > m_ref + kRescaleThreshold;  // true for the first finite page
@@ -591,7 +829,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             const float c2 = p.scale_log2;
 #if MLA_F8
             uint32_t pk[16];
-            float psum = 0.f;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float p0 = ex2_approx(fmaf(sv[4 * j], c2, neg_m));
@@ -599,18 +837,20 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 const float p2 = ex2_approx(fmaf(sv[4 * j + 2], c2, neg_m));
                 const float p3 = ex2_approx(fmaf(sv[4 * j + 3], c2, neg_m));
                 pk[j] = pack_e4m3x4(p0, p1, p2, p3);   // P <= 2^8 (lazy rescale), within e4m3's 448
-                psum += (p0 + p1) + (p2 + p3);         // fp32 terms: the denominator, and so lse, stays exact
+                ps[j & 3] += (p0 + p1) + (p2 + p3);    // fp32 terms: the denominator, and so lse, stays exact
             }
+            const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
 #else
             uint32_t pk[32];
-            float psum = 0.f;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float p0 = ex2_approx(fmaf(sv[2 * j], c2, neg_m));
                 const float p1 = ex2_approx(fmaf(sv[2 * j + 1], c2, neg_m));
                 pk[j] = pack_bf16x2(p0, p1);
-                psum += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
+                ps[j & 3] += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
             }
+            const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
 #endif
             l_sum += psum;
             // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
@@ -694,6 +934,7 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_constant__ CUtensorMap km64,
+                   const __grid_constant__ CUtensorMap kq, const __grid_constant__ CUtensorMap kqr,
                    const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -726,10 +967,10 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
             mbar_init(bar_addr(c, B_PFULL + i), 128);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c, B_XFULL + i), nwa);       // + 8 KB of DMA per arrival
+            mbar_init(bar_addr(c, B_XFULL + i), nwa);       // + a warp tile of DMA per arrival
             mbar_init(bar_addr(c, B_XINFREE + i), nwa);     // remote arrivals from the peer
         }
-        mbar_init(bar_addr(c, B_STAGEFREE), nwa);           // remote arrivals from the peer
+        for (int i = 0; i < 2; ++i) mbar_init(bar_addr(c, B_STAGEFREE + i), nwa);   // remote arrivals from the peer
         for (int i = 0; i < kPvBars; ++i) mbar_init(bar_addr(c, B_PVDONE + i), 1);
         mbar_init(bar_addr(c, B_OFINAL), 1);
         mbar_init(bar_addr(c, B_QREADY), 128);
@@ -739,6 +980,10 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
     if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&km128);
         tma_prefetch_desc(&km64);
+        if (p.q_tma) {
+            tma_prefetch_desc(&kq);
+            tma_prefetch_desc(&kqr);
+        }
     }
     if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -757,7 +1002,7 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
         exchange_role(c, p, rec, tmem, cta, rb, hk);
     } else if (warp == 8) {
         const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
-        producer_role(c, p, &km128, &km64, rec, cta, rb, hk, pol);
+        producer_role(c, p, &km128, &km64, &kq, &kqr, rec, cta, rb, hk, pol);
     } else {
         mma_role(c, p, rec, tmem, lane);
     }

@@ -3,7 +3,10 @@ kernel applies (CPU only).
 
 The model restates the kernel's arithmetic in float64 numpy on the decoded values:
 - logits from the two halves of the dot product (latent 0-255 + RoPE 512-543 and latent
-  256-511 + RoPE 544-575), added unrounded (the pair exchanges its partial sums in fp32);
+  256-511 + RoPE 544-575); each CTA of the pair adds its own half exactly and the peer's
+  half in the 16-bit block format the pair exchanges (tests/exchange_format.py), so the
+  logits behind output dims 0-255 and the lse (CTA 0) differ from those behind dims
+  256-511 (CTA 1);
 - probabilities 2^(logit * log2(e) - max), rounded to e4m3 for the PV product;
 - the denominator summing the unrounded probabilities.
 Its error against the oracle must stay inside the bar the GPU test applies, with the mean
@@ -14,6 +17,7 @@ import pytest
 import torch
 
 import tests.test_fp8_gpu as T
+from tests.exchange_format import block16
 from oracle import fp8 as F
 from oracle import reference as R
 
@@ -47,12 +51,16 @@ def test_rounding_model_stays_inside_the_bar(name, sharp, s_q, causal, Ls):
         t = np.arange(n)
         K = kv[bt[b, t // 64], t % 64, 0]
         qr = qv[b, i, h]
-        S = (K[:, h0] @ qr[h0]) + (K[:, h1] @ qr[h1])
-        lg = S * bmm1 * np.log2(np.e)
-        m = lg.max()
-        p = np.exp2(lg - m)
-        model_o[r] = T.BMM2 * (_e4m3(p)[:, None] * K[:, :512]).sum(axis=0) / p.sum()
-        model_l[r] = (m + np.log2(p.sum())) * np.log(2.0)
+        S0 = (K[:, h0] @ qr[h0]).astype(np.float32).astype(np.float64)
+        S1 = (K[:, h1] @ qr[h1]).astype(np.float32).astype(np.float64)
+        for cta, S in ((0, S0 + block16(S1)), (1, block16(S0) + S1)):
+            lg = S * bmm1 * np.log2(np.e)
+            m = lg.max()
+            p = np.exp2(lg - m)
+            d = slice(256 * cta, 256 * cta + 256)
+            model_o[r, d] = T.BMM2 * (_e4m3(p)[:, None] * K[:, d]).sum(axis=0) / p.sum()
+            if cta == 0:
+                model_l[r] = (m + np.log2(p.sum())) * np.log(2.0)
     ref_o, ref_l = F.mla_decode_fp8(q8, k8, inp.block_table, inp.cache_seqlens, bmm1, T.BMM2, causal)
     ro = ref_o.reshape(-1, 512)
     rl = ref_l.transpose(0, 2, 1).reshape(-1)
