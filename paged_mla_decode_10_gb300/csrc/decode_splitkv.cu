@@ -19,8 +19,10 @@
 // tensor core, and the two CTAs swap their partial tiles through distributed
 // shared memory.  Each CTA adds the peer's tile to its own, runs the online
 // softmax on S = S_0 + S_1 and accumulates its half of O = softmax(S) V.  The
-// fp32 O half (128 x 256) fills half of TMEM, which leaves room for two logit
-// buffers and the resident Q half.
+// fp32 O half (128 x 256) fills half of TMEM; 64 columns hold Q (half of the
+// bf16 Q half; the other 128 dims sit in shared memory) and three 64-column
+// buffers take the logits and probabilities of three pages, so QK^T runs two
+// pages ahead of PV.
 //
 // Exchange format.  A tile crosses the pair as 16-bit integers with one scale
 // per row and page (block floating point): the 64 partial logits x_j of a row
@@ -32,8 +34,10 @@
 // own half stays exact.  MLA_XEXACT = 1 builds the fp32 exchange instead.
 //
 // Per CTA:
-//   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,512) Q (bf16 pairs)
-//   smem  Q RoPE half (SW64) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
+//   TMEM  cols [0,256) O   [256,320) S0   [320,384) S1   [384,448) Q latent dims
+//         0-127 of the half (bf16 pairs)   [448,512) S2
+//   smem  Q RoPE half (SW64) | Q latent dims 128-255 of the half (two SW128
+//         boxes, 32 KB) | 4-stage page ring (4 x SW128 + 1 x SW64 boxes,
 //         36,864 B per page half) | S exchange: landing slot(s) and staging
 //         tile(s), 16,896 B each (a warp's 4,224 B of a slot are refilled as
 //         soon as the softmax warp has read them) | epilogue staging | mbarriers
@@ -52,8 +56,7 @@
 //   - the MMAs are kind::f8f6f4 (K = 32): 9 per page for QK^T, 2 for PV;
 //   - a page half is 18,432 B (two 128-dim SW128 boxes and one 32-byte SW32
 //     RoPE box), so the ring has eight stages;
-//   - Q fills TMEM columns [384,448) (e4m3 quads), which leaves [448,512) for
-//     a third S/P buffer: QK^T runs two pages ahead of PV;
+//   - the whole Q half fits in TMEM columns [384,448) (e4m3 quads);
 //   - the smaller ring leaves room for two landing slots and two staging
 //     tiles, so a page's partial tile leaves while the previous one is still
 //     crossing or being read;
@@ -87,10 +90,12 @@ namespace {
 #ifndef MLA_XEXACT
 #define MLA_XEXACT 0
 #endif
-// Landing slots for the peer's partial tiles (a slot is refilled once the softmax
-// warps have read it: XINFREE) and staging tiles for ours (one is rewritten once
-// the peer has received the tile it held: STAGEFREE).  With two of each, the tile
-// of page i leaves while that of page i - 1 is still in flight or being read.
+// A warp's partial tile is staged in shared memory (XOUT, rewritten once the peer
+// has received it: STAGEFREE) and one DMA per warp carries it into the peer's
+// landing slot (XIN, refilled once the softmax warps have read it: XINFREE).
+// With two of each, the tile of page i leaves while that of page i - 1 is still
+// in flight or being read.  (Stores straight from registers into the peer's slot,
+// st.async, were slower: they hold up the SM's other shared-memory accesses.)
 #ifndef MLA_XIN_SLOTS
 #if MLA_F8 && !MLA_XEXACT
 #define MLA_XIN_SLOTS 2
@@ -113,7 +118,7 @@ constexpr int kStages = 8;
 constexpr int kLatBoxes = 2;                    // 128 e4m3 dims (128 B rows) per latent box
 constexpr uint32_t kRopeRow = 32;               // bytes per RoPE row: 32 e4m3 dims, SW32
 #else
-constexpr int kStages = 4;
+constexpr int kStages = MLA_XEXACT ? 3 : 4;     // the fp32 exchange tiles take a stage's room
 constexpr int kLatBoxes = 4;                    // 64 bf16 dims (128 B rows) per latent box
 constexpr uint32_t kRopeRow = 64;               // bytes per RoPE row: 32 bf16 dims, SW64
 #endif
@@ -134,7 +139,16 @@ constexpr float kXUntrim = 1.0000152587890625f; // 1 + 2^-16 = 1 / (1 - 2^-16) t
 #endif
 constexpr uint32_t kXBytes = 4 * kXWarpBytes;   // one 128 x 64 partial-logit tile
 constexpr uint32_t OFF_QR = 0;                  // Q RoPE half: 128 rows x kRopeRow
-constexpr uint32_t OFF_K = 128u * kRopeRow;
+// bf16: the Q latent dims [128, 256) of the CTA's half live in shared memory (two
+// 64-dim SW128 K-major boxes of 128 rows), so that TMEM holds only 64 columns of Q
+// and has room for a third S/P buffer; e4m3 keeps its whole Q half in TMEM
+#if MLA_F8
+constexpr uint32_t kQlBytes = 0;
+#else
+constexpr uint32_t kQlBytes = 2u * 16384u;
+#endif
+constexpr uint32_t OFF_QL = 128u * kRopeRow;    // 1024-byte aligned
+constexpr uint32_t OFF_K = OFF_QL + kQlBytes;
 constexpr uint32_t OFF_XIN = OFF_K + kStages * kHalfBytes;    // peer's partial tiles land here (kXSlots)
 constexpr uint32_t OFF_XOUT = OFF_XIN + kXSlots * kXBytes;    // our partial tiles, staged for the DMA (kXOut)
 constexpr uint32_t OFF_EPI = OFF_XOUT + kXOut * kXBytes;  // epilogue staging, one tile per softmax warp
@@ -143,16 +157,10 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kThreads = 320;                   // 10 warps, roles below
-// S/P buffers in TMEM and how far QK^T runs ahead of PV: two buffers (QK^T(i)
-// waits for PV(i - 2)) beside a 128-column bf16 Q; three beside the 64-column
-// e4m3 Q (QK^T(i) waits for PV(i - 3), PV issued two pages behind QK^T).
-#if MLA_F8
+// S/P buffers in TMEM and how far QK^T runs ahead of PV: three buffers beside the
+// 64 columns of Q (QK^T(i) waits for PV(i - 3), PV issued two pages behind QK^T).
 constexpr int kSBufs = 3;
 constexpr int kPvBars = 2;   // PV completions alternate over two barriers (see the O correction)
-#else
-constexpr int kSBufs = 2;
-constexpr int kPvBars = 1;
-#endif
 constexpr int kLag = kSBufs - 1;                // PV(i) is issued after QK^T(i + kLag)
 #if MLA_F8
 constexpr int kPvKeys = 32;                     // keys per PV MMA (K step)
@@ -191,12 +199,8 @@ constexpr int B_COUNT = B_DRAIN + 1;
 static_assert(B_COUNT <= 64, "barrier area");
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;
-// first TMEM column of S/P buffer sb: 256, 320 (and 448, after the e4m3 Q)
-#if MLA_F8
+// first TMEM column of S/P buffer sb: 256, 320 and 448 (after the 64 columns of Q)
 __device__ __forceinline__ uint32_t s_col(uint32_t sb) { return sb == 2u ? 448u : TM_S + 64u * sb; }
-#else
-__device__ __forceinline__ uint32_t s_col(uint32_t sb) { return TM_S + 64u * sb; }
-#endif
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 // The CTA-scope acquire of wait_bar suffices for every barrier here: XFULL
@@ -353,9 +357,15 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
         const int nb_seq = (s.L + kPage - 1) / kPage;
         const int tail = s.L & (kPage - 1);
         const int n = s.hi - s.lo;
-        for (int j = 0; j < n; ++j, ++it, ++si) {
-            const uint32_t st = si % kStages, sb = it % kSBufs;
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (si / kStages) & 1u));
+        const uint32_t it0 = it, si0 = si;   // page and ring counters of the segment's first page
+        // PV of segment page k (over fewer K steps on a sequence's partly filled last page)
+        auto do_pv = [&](int k) -> bool {
+            const int nst = (s.lo + k == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
+            return issue_pv(c, tmem, it0 + (uint32_t)k, si0 + (uint32_t)k, k == 0, nst, lane);
+        };
+        for (int j = 0; j < n; ++j) {
+            const uint32_t sj = si0 + (uint32_t)j, st = sj % kStages, sb = (it0 + (uint32_t)j) % kSBufs;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (sj / kStages) & 1u));
             if (!ok) break;
             const uint32_t stage = c.base + OFF_K + st * kHalfBytes;
             if (s.lo + j == nb_seq - 1 && tail != 0) {
@@ -375,7 +385,7 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // Buffer sb last held S/P of page it - kSBufs; its PV was issued before
+            // Buffer sb last held S/P of page j - kSBufs; its PV was issued before
             // this S (tcgen05 MMAs of one thread execute in issue order).
             tc_fence_after();
             if (lane == 0) {
@@ -392,10 +402,17 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 const uint64_t br = make_sdesc(stage + kRopeOff, 16, 256, kSwizzle32B);
                 umma_ss_f8(dS, aq, br, idS, 1u);
 #else
+                // latent dims 0-127 of the half: A from TMEM; dims 128-255: A from the SW128
+                // Q tile in shared memory (+32 B per k-step, +16 KB per 64-dim box)
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
+                for (int kk = 0; kk < 8; ++kk)
                     umma_ts(dS, tmem + TM_Q + 8u * kk, bk + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idS,
                             kk > 0 ? 1u : 0u);
+                const uint64_t aql = make_sdesc(c.base + OFF_QL, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 8; kk < 16; ++kk)
+                    umma_ss(dS, aql + (uint64_t)(((kk - 8) >> 2) * 1024 + (kk & 3) * 2),
+                            bk + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idS, 1u);
                 const uint64_t aq = make_sdesc(c.base + OFF_QR, 16, 512, kSwizzle64B);
                 const uint64_t br = make_sdesc(stage + kRopeOff, 16, 512, kSwizzle64B);
                 umma_ss(dS, aq, br, idS, 1u);
@@ -404,21 +421,16 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 umma_commit(bar_addr(c, B_SFULL + sb));
             }
             __syncwarp();
-            if (j >= kLag) {
-                const int pg = s.lo + j - kLag;
-                const int nst = (pg == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
-                if (!issue_pv(c, tmem, it - kLag, si - kLag, j == kLag, nst, lane)) { ok = false; break; }
-            }
+            // PV of page j - kLag: issued after this QK^T, which keeps the next logit tile
+            // ahead of the softmax, and before QK^T(j + 1) reuses its S buffer
+            if (j >= kLag && !do_pv(j - kLag)) { ok = false; break; }
         }
         if (!ok) break;
-        // the segment's last kLag pages (page n - d is its first when n == d)
-#pragma unroll
-        for (int d = kLag; d >= 1; --d) {
-            const int pg = s.hi - d;
-            const int nst = (pg == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
-            if (n >= d && !issue_pv(c, tmem, it - d, si - d, n == d, nst, lane)) { ok = false; break; }
-        }
+        // the segment's last kLag pages
+        for (int k = n > kLag ? n - kLag : 0; ok && k < n; ++k) ok = do_pv(k);
         if (!ok) break;
+        it = it0 + (uint32_t)n;
+        si = si0 + (uint32_t)n;
         if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
         __syncwarp();
         ++g;
@@ -496,10 +508,16 @@ __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p,
         tmem_st_32x32b_x64(tmem_q, w);
     }
     {
+        // latent dims 128-255 of the half -> the SW128 K-major Q tile in shared memory
+        // (box bx = dims [128 + 64 bx, +64); 16-byte chunk c of row r at c ^ (r & 7))
         uint32_t w[64];
 #pragma unroll
         for (int v = 0; v < 8; ++v) load32(qrow + cta * 32 + 16 + 2 * v, &w[8 * v]);
-        tmem_st_32x32b_x64(tmem_q + 64u, w);
+        uint8_t *ql = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_QL + r * 128;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            *reinterpret_cast<uint4 *>(ql + (k >> 3) * 16384 + (((k & 7) ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 #pragma unroll
@@ -540,6 +558,17 @@ __device__ __forceinline__ bool copy_q_stages(const Ctx &c, uint32_t tmem_q, int
 #pragma unroll
         for (int bx = 0; bx < kBoxes; ++bx) {
             const uint8_t *row = stage + bx * 16384u + row_in_box;
+#if !MLA_F8
+            if (h == 1) {
+                // latent dims 128-255: the row as it is into the SW128 Q tile (same
+                // offsets within 1024-byte aligned boxes, so the swizzle carries over)
+                uint4 *dst = reinterpret_cast<uint4 *>(smem_gen + OFF_QL + bx * 16384u + row_in_box);
+                const uint4 *src = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = src[j];
+                continue;
+            }
+#endif
             uint32_t w[32];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -620,12 +649,39 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(c, B_SREAD + sb));
-            // staging buffer ob (phase oph)
+            const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
+            const uint32_t dst = xin_peer + b * kXBytes;   // the warp's tile in the peer's slot b
+#if !MLA_XEXACT
+            // the row in the 16-bit block format: one scale exponent, 64 codes.  Keys past
+            // the sequence end (rows of a partly filled last page may hold anything) are
+            // sent as 0, so that they cannot set the scale.
+            uint32_t wd[32], eb;
+            {
+                const int past = s.L - blk * kPage;
+                if (past < kPage) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) raw[j] = j < past ? raw[j] : 0u;
+                }
+                float av[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) av[j] = fabsf(__uint_as_float(raw[j]));
+                const float amax = max64(av);
+                eb = (__float_as_uint(amax) >> 23) & 255u;   // biased exponent E + 127
+                eb = eb < 15u ? 15u : (eb > 254u ? 254u : eb);
+                const float sc = __uint_as_float((268u - eb) << 23) * kXTrim;   // 2^(14-E) (1 - 2^-16)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float t0 = fmaf(__uint_as_float(raw[2 * i]), sc, kXMagic);
+                    const float t1 = fmaf(__uint_as_float(raw[2 * i + 1]), sc, kXMagic);
+                    wd[i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+                }
+            }
+#endif
+            // staged in buffer ob (phase oph), then one DMA per warp tile
             const uint32_t ob = it % kXOut, oph = (it / kXOut) & 1u;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE + ob), oph ^ 1u));
             if (!ok) break;
-            const uint32_t xfull = b ? xfull_peer[1] : xfull_peer[0];
-            const uint32_t src = c.base + OFF_XOUT + ob * kXBytes + (uint32_t)q * kXWarpBytes, dst = xin_peer + b * kXBytes;
+            const uint32_t src = c.base + OFF_XOUT + ob * kXBytes + (uint32_t)q * kXWarpBytes;
             uint8_t *const stg = half0 + ob * kXBytes;   // this lane's row in buffer ob
 #if MLA_XEXACT
             // keys 0-31 of the rows first: their 4 KB leave while keys 32-63 are staged
@@ -646,36 +702,11 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             __syncwarp();
             if (lane == 0) bulk_copy_to_peer(dst + 4096u, src + 4096u, 4096u, xfull);
 #else
-            {
-                // the row in the 16-bit block format: one scale exponent, 64 codes.  Keys
-                // past the sequence end (rows of a partly filled last page may hold
-                // anything) are sent as 0, so that they cannot set the scale.
-                const int past = s.L - blk * kPage;
-                if (past < kPage) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) raw[j] = j < past ? raw[j] : 0u;
-                }
-                float av[64];
-#pragma unroll
-                for (int j = 0; j < 64; ++j) av[j] = fabsf(__uint_as_float(raw[j]));
-                const float amax = max64(av);
-                uint32_t eb = (__float_as_uint(amax) >> 23) & 255u;   // biased exponent E + 127
-                eb = eb < 15u ? 15u : (eb > 254u ? 254u : eb);
-                const float sc = __uint_as_float((268u - eb) << 23) * kXTrim;   // 2^(14-E) (1 - 2^-16)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 8 * ch + 2 * e;
-                        const float t0 = fmaf(__uint_as_float(raw[j]), sc, kXMagic);
-                        const float t1 = fmaf(__uint_as_float(raw[j + 1]), sc, kXMagic);
-                        w4[e] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
-                    }
-                    *reinterpret_cast<uint4 *>(stg + ((ch ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-                *reinterpret_cast<uint32_t *>(stg - lane * 128u + 4096u + lane * 4u) = eb;
-            }
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(stg + ((ch ^ (lane & 7)) << 4)) =
+                    make_uint4(wd[4 * ch], wd[4 * ch + 1], wd[4 * ch + 2], wd[4 * ch + 3]);
+            *reinterpret_cast<uint32_t *>(stg - lane * 128u + 4096u + lane * 4u) = eb;
             fence_proxy_async_smem();
             __syncwarp();
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));

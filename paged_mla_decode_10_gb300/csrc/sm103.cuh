@@ -68,13 +68,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                  :: "r"(cluster_bar) : "memory");
 }
-// Asynchronous 16-byte store into another CTA's shared memory; its arrival is
-// counted (complete_tx, in bytes) on an mbarrier of that CTA.  No fence.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
-                                            uint32_t cluster_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-                 :: "r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
-}
 // Arrive on a peer CTA's barrier without ordering any memory access (a pure
 // signal: "you may reuse that buffer").
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
