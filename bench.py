@@ -330,7 +330,8 @@ def run_libmla(args, w, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     parts = M.mla_get_num_sm_parts(w.rows, w.h_k, dev)
-    md, ns = M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=parts)
+    kv_dtype = torch.float8_e4m3fn if e4m3 else None   # the schedule's segment cost follows the cache type
+    md, ns = M.mla_get_metadata(inp.cache_seqlens, w.rows, w.h_k, num_sm_parts=parts, kv_dtype=kv_dtype)
     out = torch.empty(w.batch, w.s_q, w.h_q, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.batch, w.h_q, w.s_q, dtype=torch.float32, device=dev)
     shape = M.make_shape(q_in, k_in, inp.block_table, out.stride()[:3], parts, 512)
@@ -413,9 +414,10 @@ def run_libmla(args, w, world, rank, local):
     torch.cuda._sleep(2_000_000)
     em0.record(stream)
     for _ in range(n_md):
-        M._lib.check(L_md.mla_get_metadata(ctypes.c_void_p(inp.cache_seqlens.data_ptr()), w.batch, w.rows, w.h_k, parts,
-                                           ctypes.c_void_p(md_buf.data_ptr()), ctypes.c_void_p(ns_buf.data_ptr()),
-                                           ctypes.c_void_p(stream.cuda_stream)), "mla_get_metadata")
+        M._lib.check(L_md.mla_get_metadata_ex(ctypes.c_void_p(inp.cache_seqlens.data_ptr()), w.batch, w.rows, w.h_k,
+                                              1 if e4m3 else 2, parts, ctypes.c_void_p(md_buf.data_ptr()),
+                                              ctypes.c_void_p(ns_buf.data_ptr()), ctypes.c_void_p(stream.cuda_stream)),
+                     "mla_get_metadata_ex")
     em1.record(stream)
     torch.cuda.synchronize()
     metadata_us = 1e3 * em0.elapsed_time(em1) / n_md
@@ -455,7 +457,7 @@ def run_libmla(args, w, world, rank, local):
             q_d.copy_(q_h, non_blocking=True)
             bt_d.copy_(bt_h, non_blocking=True)
             L_d.copy_(L_h, non_blocking=True)
-            md_d, ns_d = M.mla_get_metadata(L_d, w.rows, w.h_k, num_sm_parts=parts)
+            md_d, ns_d = M.mla_get_metadata(L_d, w.rows, w.h_k, num_sm_parts=parts, kv_dtype=kv_dtype)
             M.mla_decode_fwd_fp8(q_d, k_in, bt_d, L_d, 512, md_d, ns_d, inp.scale, 1.0, **call_f8)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)

@@ -126,8 +126,10 @@ int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, 
  * num_blocks, 0, 0]; the part processes, for b in [begin_b, end_b], blocks
  * [b == begin_b ? begin_blk : 0, b == end_b ? end_blk : ceil(L_b / 64)).
  * Policy: greedy contiguous walk over (sequence, block) with a fixed cost of
- * 6 blocks per segment and a per-part target of
- * ceil((W + (num_sm_parts - 1) * 6) / num_sm_parts), W = sum(n_b + 6).
+ * c blocks per segment and a per-part target of
+ * ceil((W + (num_sm_parts - 1) * c) / num_sm_parts), W = sum(n_b + c), where
+ * c (the decode kernel's fixed work per segment in page times) is 6 for
+ * num_heads_per_head_k >= 64 and 4 below, for a bf16 cache.
  * Errors: MLA_ERR_ARG (NULL pointer, batch < 0, num_sm_parts < 1,
  * num_heads_per_head_k < 1, num_heads_k < 1), MLA_ERR_UNSUPPORTED
  * (batch > 16384 or num_sm_parts > 1024), MLA_ERR_CUDA.
@@ -135,6 +137,17 @@ int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, 
 int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k,
                      int num_heads_k, int num_sm_parts, int32_t *tile_scheduler_metadata,
                      int32_t *num_splits, mla_stream_t stream);
+
+/*
+ * mla_get_metadata for a cache of kv_bytes-byte elements (2: bf16, 1: e4m3,
+ * for mla_decode_fwd_fp8): the segment cost c is one block more for e4m3,
+ * whose pages take less time against the same fixed work.  Any schedule is
+ * valid for either call; this one balances the parts for that cache.
+ * Errors: as mla_get_metadata, and MLA_ERR_ARG for kv_bytes other than 1 or 2.
+ */
+int mla_get_metadata_ex(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k,
+                        int num_heads_k, int kv_bytes, int num_sm_parts, int32_t *tile_scheduler_metadata,
+                        int32_t *num_splits, mla_stream_t stream);
 
 /*
  * Bytes of workspace mla_decode_fwd needs for `shape`: fp32 partial outputs

@@ -19,7 +19,9 @@ A part covers, for b in [begin_b, end_b] (b < batch), the blocks
 where n_b = ceil(max(L_b, 0) / 64); an empty range is no segment.
 
 Policy (greedy contiguous walk with a fixed cost per segment):
-  c = FIXED_COST blocks charged for every segment a part opens
+  c = blocks charged for every segment a part opens: segment_cost(R, kv_bytes)
+      = 6 for R >= 64 query rows per KV head, 4 below, plus 1 for a one-byte
+      (e4m3) cache; FIXED_COST = 6 is the bf16 value for R >= 64
   W = sum over b with n_b > 0 of (n_b + c)
   T = max(1, ceil((W + (parts - 1) * c) / parts))
   parts take the blocks in (b, blk) order; part p stops opening segments once
@@ -42,6 +44,13 @@ PAGE = 64
 # measured on the decode kernel as about six pages' time.
 FIXED_COST = 6
 RECORD = 8
+
+
+def segment_cost(rows_per_head_k: int, kv_bytes: int = 2) -> int:
+    """Blocks charged per segment: a part's fixed work for a sequence it takes up,
+    in page times -- larger with many query rows (more output to store), and one more
+    for an e4m3 cache, whose pages take less time than bf16 ones."""
+    return (6 if rows_per_head_k >= 64 else 4) + (1 if kv_bytes == 1 else 0)
 
 
 def n_blocks(seqlens: Sequence[int]) -> List[int]:

@@ -73,6 +73,7 @@ def load():
     L.mla_last_error.restype = ctypes.c_char_p
     L.mla_get_num_sm_parts.argtypes = [c_int, c_int, c_int, ctypes.POINTER(c_int)]
     L.mla_get_metadata.argtypes = [vp, c_int, c_int, c_int, c_int, vp, vp, vp]
+    L.mla_get_metadata_ex.argtypes = [vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp]
     L.mla_workspace_size.argtypes = [sp, ctypes.POINTER(c_size)]
     dec = [sp, vp, vp, vp, vp, vp, vp, ctypes.c_float, c_int, vp, vp, vp, c_size, vp]
     for name in ("mla_decode_fwd", "mla_decode_splitkv", "mla_decode_combine"):
@@ -92,7 +93,8 @@ def load():
     L.mla_check_device_error.argtypes = [ctypes.POINTER(c_int), c_int]
     L.mla_shutdown.argtypes = []
     L.mla_shutdown.restype = c_int
-    for name in ("mla_get_num_sm_parts", "mla_get_metadata", "mla_workspace_size", "mla_check_device_error"):
+    for name in ("mla_get_num_sm_parts", "mla_get_metadata", "mla_get_metadata_ex", "mla_workspace_size",
+                 "mla_check_device_error"):
         getattr(L, name).restype = c_int
     _lib = L
     return L

@@ -50,8 +50,11 @@ def mla_get_num_sm_parts(num_heads_per_head_k: int, num_heads_k: int, device=Non
 
 
 def mla_get_metadata(cache_seqlens: torch.Tensor, num_heads_per_head_k: int, num_heads_k: int,
-                     num_sm_parts: Optional[int] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Split-KV schedule: (tile_scheduler_metadata (parts, 8) int32, num_splits (B+1) int32)."""
+                     num_sm_parts: Optional[int] = None, stream=None,
+                     kv_dtype: Optional[torch.dtype] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split-KV schedule: (tile_scheduler_metadata (parts, 8) int32, num_splits (B+1) int32).
+    kv_dtype: the cache's element type (None or bfloat16: mla_get_metadata; float8_e4m3fn:
+    mla_get_metadata_ex with one-byte elements)."""
     L = _lib.load()
     _require(cache_seqlens.is_cuda and cache_seqlens.dtype == torch.int32 and cache_seqlens.dim() == 1,
              "cache_seqlens must be a 1-D int32 CUDA tensor")
@@ -61,8 +64,13 @@ def mla_get_metadata(cache_seqlens: torch.Tensor, num_heads_per_head_k: int, num
     B = cache_seqlens.shape[0]
     md = torch.empty((num_sm_parts, _lib.MLA_METADATA_SIZE), dtype=torch.int32, device=cache_seqlens.device)
     ns = torch.empty((B + 1,), dtype=torch.int32, device=cache_seqlens.device)
-    check(L.mla_get_metadata(_ptr(cache_seqlens), B, int(num_heads_per_head_k), int(num_heads_k),
-                             int(num_sm_parts), _ptr(md), _ptr(ns), _stream(stream)), "mla_get_metadata")
+    if kv_dtype is None or kv_dtype == torch.bfloat16:
+        check(L.mla_get_metadata(_ptr(cache_seqlens), B, int(num_heads_per_head_k), int(num_heads_k),
+                                 int(num_sm_parts), _ptr(md), _ptr(ns), _stream(stream)), "mla_get_metadata")
+    else:
+        _require(kv_dtype in (torch.float8_e4m3fn, torch.uint8), "kv_dtype must be bfloat16 or float8_e4m3fn")
+        check(L.mla_get_metadata_ex(_ptr(cache_seqlens), B, int(num_heads_per_head_k), int(num_heads_k), 1,
+                                    int(num_sm_parts), _ptr(md), _ptr(ns), _stream(stream)), "mla_get_metadata_ex")
     return md, ns
 
 

@@ -21,7 +21,8 @@ __global__ void mla_splitkv_kernel_f8(const __grid_constant__ CUtensorMap km128,
                                       const __grid_constant__ CUtensorMap km64, const __grid_constant__ CUtensorMap kq,
                                       const __grid_constant__ CUtensorMap kqr, const __grid_constant__ DecodeParams p);
 __global__ void mla_combine_kernel(const __grid_constant__ DecodeParams p);
-__global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits);
+__global__ void mla_metadata_kernel(const int32_t *seqlens, int batch, int parts, int cost, int32_t *md,
+                                    int32_t *num_splits);
 size_t metadata_smem_bytes(int batch, int parts);
 uint32_t splitkv_smem_bytes();
 uint32_t splitkv_f8_smem_bytes();
@@ -521,9 +522,10 @@ int launch_combine(const mla_shape_t *sh, const Prepared &pr, cudaStream_t strea
     return MLA_OK;
 }
 
-int launch_metadata(const int32_t *seqlens, int batch, int parts, int32_t *md, int32_t *num_splits,
+int launch_metadata(const int32_t *seqlens, int batch, int parts, int cost, int32_t *md, int32_t *num_splits,
                     cudaStream_t stream) {
-    mla_metadata_kernel<<<1, 256, metadata_smem_bytes(batch, parts), stream>>>(seqlens, batch, parts, md, num_splits);
+    mla_metadata_kernel<<<1, 256, metadata_smem_bytes(batch, parts), stream>>>(seqlens, batch, parts, cost, md,
+                                                                              num_splits);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "metadata launch");
     return MLA_OK;
@@ -674,18 +676,26 @@ int mla_get_num_sm_parts(int device, int num_heads_per_head_k, int num_heads_k, 
 
 int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k, int num_heads_k,
                      int num_sm_parts, int32_t *tile_scheduler_metadata, int32_t *num_splits, mla_stream_t stream) {
+    return mla_get_metadata_ex(cache_seqlens, batch, num_heads_per_head_k, num_heads_k, 2, num_sm_parts,
+                               tile_scheduler_metadata, num_splits, stream);
+}
+
+int mla_get_metadata_ex(const int32_t *cache_seqlens, int batch, int num_heads_per_head_k, int num_heads_k,
+                        int kv_bytes, int num_sm_parts, int32_t *tile_scheduler_metadata, int32_t *num_splits,
+                        mla_stream_t stream) {
     if (!tile_scheduler_metadata || !num_splits || (batch > 0 && !cache_seqlens))
         return fail(MLA_ERR_ARG, "mla_get_metadata: NULL pointer");
     if (batch < 0 || num_sm_parts < 1 || num_heads_per_head_k < 1 || num_heads_k < 1)
         return fail(MLA_ERR_ARG, "mla_get_metadata: bad argument");
+    if (kv_bytes != 1 && kv_bytes != 2) return fail(MLA_ERR_ARG, "mla_get_metadata_ex: kv_bytes must be 1 or 2");
     if (batch > kMaxBatchMetadata) return fail(MLA_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatchMetadata);
     if (num_sm_parts > kMaxPartsMetadata)
         return fail(MLA_ERR_UNSUPPORTED, "num_sm_parts %d > %d", num_sm_parts, kMaxPartsMetadata);
     DeviceState *ds = nullptr;
     int st = device_state(&ds);
     if (st != MLA_OK) return st;
-    return launch_metadata(cache_seqlens, batch, num_sm_parts, tile_scheduler_metadata, num_splits,
-                           reinterpret_cast<cudaStream_t>(stream));
+    return launch_metadata(cache_seqlens, batch, num_sm_parts, segment_cost(num_heads_per_head_k, kv_bytes),
+                           tile_scheduler_metadata, num_splits, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_workspace_size(const mla_shape_t *shape, size_t *bytes) {
@@ -898,7 +908,9 @@ int mla_decode_fwd_host(const mla_shape_t *shape, const void *q_host, const void
     if ((e = cudaMemcpyAsync(L_d, cache_seqlens_host, lay.size[kStLen], cudaMemcpyHostToDevice, h->side)) != cudaSuccess ||
         (e = cudaMemcpyAsync(bt_d, block_table_host, lay.size[kStBt], cudaMemcpyHostToDevice, h->side)) != cudaSuccess)
         return cuda_fail(e, "copy of cache_seqlens / block_table");
-    if ((st = launch_metadata(L_d, sh.batch, sh.num_sm_parts, md_d, ns_d, h->side)) != MLA_OK) return st;
+    const int rows = (int)((long long)sh.s_q * sh.h_q / sh.h_k);
+    if ((st = launch_metadata(L_d, sh.batch, sh.num_sm_parts, segment_cost(rows, 2), md_d, ns_d, h->side)) != MLA_OK)
+        return st;
     if ((e = cudaEventRecord(h->join, h->side)) != cudaSuccess) return cuda_fail(e, "join event");
     // this stream: q in, wait for the schedule, decode, results out
     if ((e = cudaMemcpyAsync(q_d, q_host, lay.size[kStQ], cudaMemcpyHostToDevice, s)) != cudaSuccess)

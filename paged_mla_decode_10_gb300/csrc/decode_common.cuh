@@ -9,7 +9,14 @@ constexpr int kPage = 64;          // cache rows per physical block
 constexpr int kDqk = 576;          // q / cache row dims (512 latent + 64 RoPE)
 constexpr int kDv = 512;           // V dims (prefix of each cache row)
 constexpr int kMdSize = 8;         // int32 per scheduler record
-constexpr int kFixedCost = 6;      // schedule: cost of opening a segment, in blocks
+// Schedule: the cost of opening a segment, in 64-row blocks -- a part's fixed work
+// for each sequence it takes up (the query load, the pipeline refill and the output
+// store), measured on the decode kernel against its page time: about 6 pages with 64
+// or more query rows per KV head, about 4 with fewer; one more with an e4m3 cache,
+// whose pages take less time than bf16 ones.
+__host__ __device__ constexpr int segment_cost(int rows_per_head_k, int kv_bytes) {
+    return (rows_per_head_k >= 64 ? 6 : 4) + (kv_bytes == 1 ? 1 : 0);
+}
 constexpr int kRowsPerBlock = 128; // query rows per CTA (tcgen05 M)
 
 // Device-side error bits (mirror MLA_DEVERR_* of the public header).

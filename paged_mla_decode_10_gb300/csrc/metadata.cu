@@ -6,7 +6,8 @@
 // The record and policy are this library's:
 //
 //   record of part p: [begin_b, begin_blk, end_b, end_blk, first_slot, num_blocks, 0, 0]
-//   n_b = ceil(max(L_b, 0) / 64); c = 6 (cost of opening a segment, in blocks)
+//   n_b = ceil(max(L_b, 0) / 64); c = cost of opening a segment, in blocks
+//   (segment_cost: 6 with >= 64 query rows per KV head, 4 with fewer, +1 for e4m3)
 //   W = sum_{n_b > 0} (n_b + c);  T = max(1, ceil((W + (parts - 1) c) / parts))
 //   parts walk the (b, blk) sequence in order; a part stops opening segments
 //   when T - load - c <= 0, takes min(remaining, T - load - c) blocks when it
@@ -87,11 +88,11 @@ __device__ __forceinline__ int last_le(int n, long long x, F at) {
 // Where a part that starts at cost position g stops, given its stop sequence
 // j (C[j] = cj, C[j + 1] = cj1): end (eb, ek), the end's cost position eg and
 // whether it is a snap (ends at a sequence start).
-__device__ __forceinline__ void part_end(long long g, long long T, int j, long long cj, long long cj1, int &eb,
-                                         int &ek, long long &eg, bool &snap) {
+__device__ __forceinline__ void part_end(long long g, long long T, long long c, int j, long long cj, long long cj1,
+                                         int &eb, int &ek, long long &eg, bool &snap) {
     const long long start = cj > g ? cj : g;                 // cost position where the part enters j
-    const long long avail = g + T - kFixedCost - start;      // blocks it may take from j
-    const long long rem = cj1 - kFixedCost - start;          // blocks of j left
+    const long long avail = g + T - c - start;               // blocks it may take from j
+    const long long rem = cj1 - c - start;                   // blocks of j left
     eb = j; ek = 0; eg = cj; snap = true;                    // no budget to open j
     if (avail > 0) {
         if (rem == avail) { eb = j + 1; eg = cj1; }          // takes the rest of j exactly
@@ -105,7 +106,7 @@ __device__ __forceinline__ void part_end(long long g, long long T, int j, long l
 // block of each part), E[batch + 1] (non-empty sequences before each
 // sequence), pb/pk[parts + 1] (part boundaries as (sequence, block)).
 __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t *__restrict__ seqlens, int batch,
-                                                                  int parts, int32_t *__restrict__ md,
+                                                                  int parts, int cost, int32_t *__restrict__ md,
                                                                   int32_t *__restrict__ num_splits) {
     extern __shared__ long long smd[];
     long long *C = smd;                                            // batch + 1
@@ -117,7 +118,8 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
     const int tid = threadIdx.x, lane = tid & 31;
     constexpr long long kMask = (1ll << kPackShift) - 1;
     // first global block of sequence i
-    auto pre = [&](int i) -> long long { return C[i] - (long long)kFixedCost * E[i]; };
+    const long long c = cost;   // cost of opening a segment, in blocks
+    auto pre = [&](int i) -> long long { return C[i] - c * E[i]; };
 
     // ---- block counts; one scan gives the block prefix and the non-empty count prefix
     const int per = (batch + kThreadsMd - 1) / kThreadsMd;
@@ -134,13 +136,13 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
         const int L = max(seqlens[b], 0);
         const long long n = ((long long)L + kPage - 1) / kPage;
         E[b] = (int32_t)(off >> kPackShift);
-        C[b] = (off & kMask) + (long long)kFixedCost * E[b];
+        C[b] = (off & kMask) + (long long)c * E[b];
         off += n + (n > 0 ? (1ll << kPackShift) : 0);
     }
-    const long long W = (total & kMask) + (long long)kFixedCost * (total >> kPackShift);
+    const long long W = (total & kMask) + (long long)c * (total >> kPackShift);
     if (tid == 0) { E[batch] = (int32_t)(total >> kPackShift); C[batch] = W; }
     __syncthreads();
-    const long long Tl = (W + (long long)(parts - 1) * kFixedCost + parts - 1) / parts;
+    const long long Tl = (W + (long long)(parts - 1) * c + parts - 1) / parts;
     const long long T = Tl < 1 ? 1 : Tl;
 
     // ---- part boundaries: warp 0
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
                 bool snap = true;      // no stop: the part takes everything left
                 if (mask) {
                     const int i = __ffs(mask) - 1;
-                    part_end(g0, T, j, j < batch ? C[j] : 0, cj1, eb, ek, eg, snap);
+                    part_end(g0, T, c, j, j < batch ? C[j] : 0, cj1, eb, ek, eg, snap);
                     eb = __shfl_sync(0xffffffffu, eb, i);
                     ek = __shfl_sync(0xffffffffu, ek, i);
                     eg = __shfl_sync(0xffffffffu, eg, i);
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
             }
             // a round: lane m takes part p + m (parts p .. parts - 2 are walked; the last takes the rest)
             const int lim = parts - 1 - p;
-            const long long g = g0 + (long long)lane * (T - kFixedCost);
+            const long long g = g0 + (long long)lane * (T - c);
             int lo = cb + 1, hi = batch + 1;   // first i with C[i] >= g + T; the stop sequence is i - 1
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
             int eb = batch, ek = 0;
             long long eg = W;
             bool snap = true;
-            if (lo <= batch) part_end(g, T, lo - 1, C[lo - 1], C[lo], eb, ek, eg, snap);
+            if (lo <= batch) part_end(g, T, c, lo - 1, C[lo - 1], C[lo], eb, ek, eg, snap);
             const unsigned mask = __ballot_sync(0xffffffffu, lane < lim && snap);
             const int last = mask ? __ffs(mask) - 1 : min(31, lim - 1);
             if (lane <= last) { pb[p + lane + 1] = eb; pk[p + lane + 1] = ek; }

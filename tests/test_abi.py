@@ -88,6 +88,9 @@ def test_metadata_rejects_bad_arguments(lib):
     dummy = ctypes.c_void_p(256)
     assert lib.mla_get_metadata(dummy, -1, 128, 1, 76, dummy, dummy, None) == 1
     assert lib.mla_get_metadata(dummy, 4, 128, 1, 0, dummy, dummy, None) == 1
+    # the one-byte / two-byte cache variant: any other element size is an argument error
+    assert lib.mla_get_metadata_ex(dummy, 4, 128, 1, 3, 76, dummy, dummy, None) == 1
+    assert lib.mla_get_metadata_ex(None, 4, 128, 1, 1, 76, None, None, None) == 1
 
 
 def test_host_decode_rejects_bad_arguments_before_any_cuda_call(lib):

@@ -77,11 +77,14 @@ def test_metadata_matches_policy_bit_exact():
              ([4096] * 128, 38), ([7], 200)]
     for Ls, parts in cases:
         L = torch.tensor([int(x) for x in Ls], dtype=torch.int32, device="cuda")
-        md, ns = M.mla_get_metadata(L, 128, 1, num_sm_parts=parts)
-        md_ref, ns_ref = OM.schedule([int(x) for x in Ls], parts)
-        np.testing.assert_array_equal(md.cpu().numpy(), md_ref)
-        np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
-        OM.check_metadata([int(x) for x in Ls], md.cpu().numpy(), ns.cpu().numpy())
+        # the four segment costs: 128 and 16 query rows per KV head, bf16 and e4m3 caches
+        for rows, kv in ((128, None), (128, torch.float8_e4m3fn), (16, None), (16, torch.float8_e4m3fn)):
+            md, ns = M.mla_get_metadata(L, rows, 1, num_sm_parts=parts, kv_dtype=kv)
+            cost = OM.segment_cost(rows, 1 if kv is not None else 2)
+            md_ref, ns_ref = OM.schedule([int(x) for x in Ls], parts, fixed_cost=cost)
+            np.testing.assert_array_equal(md.cpu().numpy(), md_ref)
+            np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
+            OM.check_metadata([int(x) for x in Ls], md.cpu().numpy(), ns.cpu().numpy())
 
 
 def test_metadata_bit_exact_on_random_small_cases():
@@ -98,8 +101,9 @@ def test_metadata_bit_exact_on_random_small_cases():
         parts = int(rng.integers(1, 100))
         Ls = [int(x) for x in L]
         Lt = torch.tensor(Ls, dtype=torch.int32, device="cuda")
-        md, ns = M.mla_get_metadata(Lt, 128, 1, num_sm_parts=parts)
-        md_ref, ns_ref = OM.schedule(Ls, parts)
+        rows, kv = ((128, None), (16, None), (128, torch.float8_e4m3fn), (16, torch.float8_e4m3fn))[trial % 4]
+        md, ns = M.mla_get_metadata(Lt, rows, 1, num_sm_parts=parts, kv_dtype=kv)
+        md_ref, ns_ref = OM.schedule(Ls, parts, fixed_cost=OM.segment_cost(rows, 1 if kv is not None else 2))
         np.testing.assert_array_equal(md.cpu().numpy(), md_ref, err_msg=f"trial {trial} L={Ls} parts={parts}")
         np.testing.assert_array_equal(ns.cpu().numpy(), ns_ref)
 

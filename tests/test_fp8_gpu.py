@@ -43,7 +43,7 @@ def _run(inp, q8, k8, parts=None, bmm1=BMM1):
     import paged_mla_decode_10_gb300 as M
     w = inp.workload
     L, bt = inp.cache_seqlens.cuda(), inp.block_table.cuda()
-    md, ns = M.mla_get_metadata(L, w.rows, w.h_k, num_sm_parts=parts)
+    md, ns = M.mla_get_metadata(L, w.rows, w.h_k, num_sm_parts=parts, kv_dtype=torch.float8_e4m3fn)
     out, lse = M.mla_decode_fwd_fp8(q8.cuda(), k8.cuda(), bt, L, 512, md, ns, bmm1, BMM2, causal=w.causal)
     torch.cuda.synchronize()
     return out, lse
