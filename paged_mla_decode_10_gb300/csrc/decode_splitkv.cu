@@ -211,9 +211,10 @@ constexpr float kRescaleThreshold = 8.0f;        // log2 units
 // ----------------------------------------------------------------------------
 // TMA producer (whole warp 8): gathers this CTA's half of every page of the
 // part.  The warp reads the block-table entries of up to 32 pages with one
-// coalesced load and lane 0 issues the copies.  When the walk enters a new
-// segment, the warp asks L2 for that segment's query rows, so that the
-// softmax warps' Q loads at the segment switch hit L2.
+// coalesced load and lane 0 issues the copies.  A segment's query half comes
+// first, by TMA through two ring stages (when the query's head layout fits a
+// box: q_tma); otherwise the warp asks L2 for the segment's query rows, so that
+// the exchange warps' own loads of them at the segment switch hit L2.
 // ----------------------------------------------------------------------------
 __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtensorMap *km128,
                               const CUtensorMap *km64, const CUtensorMap *kq, const CUtensorMap *kqr,
@@ -442,11 +443,13 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
 }
 
 // ----------------------------------------------------------------------------
-// Q of a segment, loaded by the exchange warps: this CTA's 256 latent dims ->
-// TMEM (bf16 pairs, the A operand of the QK^T MMAs), its 32 RoPE dims -> smem
-// (SW64).  Warp 4+q moves query rows 32q..32q+31 (TMEM lane quadrant q), lane
-// l row 32q + l.  Every load is issued before the first store, so a row
-// arrives in one round trip (an L2 hit after the producer's prefetch).
+// Q of a segment, loaded by the exchange warps when it cannot come by TMA:
+// this CTA's 256 latent dims -> TMEM (e4m3: all of them; bf16: dims 0-127 as
+// bf16 pairs, dims 128-255 into the SW128 Q tile in smem), its 32 RoPE dims ->
+// smem (SW64 / SW32).  Warp 4+q moves query rows 32q..32q+31 (TMEM lane
+// quadrant q), lane l row 32q + l.  Every load is issued before the first
+// store, so a row arrives in one round trip (an L2 hit after the producer's
+// prefetch).
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void load_q_half(const Ctx &c, const DecodeParams &p, uint32_t tmem_q, int q, int lane,
                                             int rb, int cta, int hk, const Segment &sg) {
@@ -595,8 +598,9 @@ __device__ __forceinline__ bool copy_q_stages(const Ctx &c, uint32_t tmem_q, int
 // ----------------------------------------------------------------------------
 // Exchange warps (4-7): ship this CTA's partial logit tile to the peer CTA.
 // Warp 4+q owns TMEM lane quadrant q, thread (4+q, l) row r = 32q + l: it
-// copies its row of S out of TMEM into the staging tile XOUT, and lane 0
-// hands the warp's 32 rows (8 KB) to the DMA engine, which writes them into
+// copies its row of S out of TMEM, encodes it (16-bit block format, or fp32
+// with MLA_XEXACT) into the staging tile XOUT, and lane 0 hands the warp's 32
+// rows (4,224 B; 8 KB in fp32) to the DMA engine, which writes them into
 // the peer's XIN slot and counts the bytes on the peer's XFULL.  The DMA, not
 // the SM's load/store pipe, carries the traffic.  XOUT is rewritten once the
 // peer has received the previous tile (STAGEFREE); an XIN slot once the peer
@@ -609,8 +613,6 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
-    // the partial logits cross between the pair in fp32 for both input types: rounding them
-    // would move each logit by up to 2^-8 of the partial sums, well above the lse tolerance
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * kXWarpBytes, peer);
     const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
@@ -757,7 +759,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     const uint32_t peer = (uint32_t)(cta ^ 1);
 
     // shared addresses
-    // this row in the landing slots: warp block of 8 KB = [column half][32 rows][128 B]
+    // this row in the landing slots: warp block of kXWarpBytes = [32 rows][128 B] + scale words
+    // (fp32: [column half][32 rows][128 B])
     const uint32_t xrow_local[2] = {c.base + OFF_XIN + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u,
                                     c.base + OFF_XIN + kXBytes + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u};
     const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE), peer),
