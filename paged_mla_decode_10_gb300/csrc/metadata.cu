@@ -184,10 +184,15 @@ __global__ void __launch_bounds__(kThreadsMd) mla_metadata_kernel(const int32_t 
                 const int mid = (lo + hi) >> 1;
                 if (C[mid] >= g + T) hi = mid; else lo = mid + 1;
             }
-            int eb = batch, ek = 0;
-            long long eg = W;
-            bool snap = true;
-            if (lo <= batch) part_end(g, T, c, lo - 1, C[lo - 1], C[lo], eb, ek, eg, snap);
+            // the part's end, computed by every lane (no divergent branch around the loads):
+            // a lane whose part takes everything left keeps the end (batch, 0)
+            const bool stops = lo <= batch;
+            const int j = stops ? lo - 1 : batch - 1;   // cb < batch, so batch >= 1
+            int eb, ek;
+            long long eg;
+            bool snap;
+            part_end(g, T, c, j, C[j], C[j + 1], eb, ek, eg, snap);
+            if (!stops) { eb = batch; ek = 0; eg = W; snap = true; }
             const unsigned mask = __ballot_sync(0xffffffffu, lane < lim && snap);
             const int last = mask ? __ffs(mask) - 1 : min(31, lim - 1);
             if (lane <= last) { pb[p + lane + 1] = eb; pk[p + lane + 1] = ek; }
