@@ -47,7 +47,9 @@
 //   warps 4-7  logit exchange: S out of TMEM, staged, DMA'd to the peer
 //   warp  8    TMA producer: a segment's Q, then its pages (block_table
 //              gather), through the same ring
-//   warp  9    MMA issuer (one lane) + TMEM allocation
+//   warp  9    QK^T issuer (one lane) + TMEM allocation
+//   warp 10    PV issuer (one lane): a second issuing thread, so that a page's PV
+//              runs on the tensor pipe beside the next pages' QK^T
 //
 // e4m3 variant.  The same source compiled with MLA_F8=1 (decode_splitkv_fp8.cu)
 // gives mla_splitkv_kernel_f8 for an e4m3 query and cache with the two fused
@@ -156,12 +158,11 @@ constexpr uint32_t OFF_BAR = OFF_EPI + 4 * kEpiWarpBytes;
 constexpr uint32_t OFF_MISC = OFF_BAR + 64 * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr int kThreads = 320;                   // 10 warps, roles below
+constexpr int kThreads = 352;                   // 11 warps, roles below
 // S/P buffers in TMEM and how far QK^T runs ahead of PV: three buffers beside the
 // 64 columns of Q (QK^T(i) waits for PV(i - 3), PV issued two pages behind QK^T).
 constexpr int kSBufs = 3;
 constexpr int kPvBars = 2;   // PV completions alternate over two barriers (see the O correction)
-constexpr int kLag = kSBufs - 1;                // PV(i) is issued after QK^T(i + kLag)
 #if MLA_F8
 constexpr int kPvKeys = 32;                     // keys per PV MMA (K step)
 #else
@@ -194,8 +195,10 @@ constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received the tile of
 constexpr int B_PVDONE = B_STAGEFREE + 2;      // kPvBars of them, page i on PVDONE + i % kPvBars
 constexpr int B_OFINAL = B_PVDONE + kPvBars;
 constexpr int B_QREADY = B_OFINAL + 1;
-constexpr int B_DRAIN = B_QREADY + 1;
-constexpr int B_COUNT = B_DRAIN + 1;
+constexpr int B_DRAIN = B_QREADY + 1;             // the QK^T thread's MMAs have completed
+constexpr int B_DRAIN_PV = B_DRAIN + 1;           // the PV thread's MMAs have completed
+constexpr int B_SFREE = B_DRAIN_PV + 1;           // kSBufs: PV of the buffer's page done, QK^T may rewrite it
+constexpr int B_COUNT = B_SFREE + kSBufs;
 static_assert(B_COUNT <= 64, "barrier area");
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;
@@ -327,6 +330,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx &c, uint32_t tmem, uint32_t i
 #endif
         umma_commit(bar_addr(c, B_KEMPTY + st));
         umma_commit(bar_addr(c, B_PVDONE + i % kPvBars));
+        umma_commit(bar_addr(c, B_SFREE + pb));
     }
     __syncwarp();
     return true;
@@ -359,14 +363,12 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
         const int tail = s.L & (kPage - 1);
         const int n = s.hi - s.lo;
         const uint32_t it0 = it, si0 = si;   // page and ring counters of the segment's first page
-        // PV of segment page k (over fewer K steps on a sequence's partly filled last page)
-        auto do_pv = [&](int k) -> bool {
-            const int nst = (s.lo + k == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
-            return issue_pv(c, tmem, it0 + (uint32_t)k, si0 + (uint32_t)k, k == 0, nst, lane);
-        };
         for (int j = 0; j < n; ++j) {
-            const uint32_t sj = si0 + (uint32_t)j, st = sj % kStages, sb = (it0 + (uint32_t)j) % kSBufs;
+            const uint32_t ij = it0 + (uint32_t)j, sj = si0 + (uint32_t)j, st = sj % kStages, sb = ij % kSBufs;
             ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_KFULL + st), (sj / kStages) & 1u));
+            if (!ok) break;
+            // S buffer sb last held page ij - kSBufs: its PV (issued by the PV thread) has completed
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFREE + sb), ((ij / kSBufs) & 1u) ^ 1u));
             if (!ok) break;
             const uint32_t stage = c.base + OFF_K + st * kHalfBytes;
             if (s.lo + j == nb_seq - 1 && tail != 0) {
@@ -386,8 +388,6 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // Buffer sb last held S/P of page j - kSBufs; its PV was issued before
-            // this S (tcgen05 MMAs of one thread execute in issue order).
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t dS = tmem + s_col(sb);
@@ -422,24 +422,51 @@ __device__ void mma_role(const Ctx &c, const DecodeParams &p, const int32_t *rec
                 umma_commit(bar_addr(c, B_SFULL + sb));
             }
             __syncwarp();
-            // PV of page j - kLag: issued after this QK^T, which keeps the next logit tile
-            // ahead of the softmax, and before QK^T(j + 1) reuses its S buffer
-            if (j >= kLag && !do_pv(j - kLag)) { ok = false; break; }
         }
-        if (!ok) break;
-        // the segment's last kLag pages
-        for (int k = n > kLag ? n - kLag : 0; ok && k < n; ++k) ok = do_pv(k);
         if (!ok) break;
         it = it0 + (uint32_t)n;
         si = si0 + (uint32_t)n;
-        if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
-        __syncwarp();
         ++g;
     }
-    // Drain: every MMA issued must complete before TMEM is freed.
+    // Drain: every MMA this thread issued must complete before TMEM is freed.
     if (lane == 0) umma_commit(bar_addr(c, B_DRAIN));
     __syncwarp();
     drain_bar(c, bar_addr(c, B_DRAIN), 0);
+}
+
+// ----------------------------------------------------------------------------
+// PV issuer (warp 10, one lane): the PV MMAs of every page, in page order, as
+// soon as the softmax warps have stored its P.  A second issuing thread lets the
+// tensor pipe run a page's PV beside the next pages' QK^T, whose N = 64 steps a
+// single thread cannot issue at the pipe's rate.  Each PV releases its ring
+// stage (KEMPTY), its S/P buffer (SFREE) and reports on PVDONE; the segment's
+// last one commits OFINAL.
+// ----------------------------------------------------------------------------
+__device__ void pv_role(const Ctx &c, const DecodeParams &p, const int32_t *rec, uint32_t tmem, int lane) {
+    SegmentWalk walk;
+    walk.init(rec);
+    Segment s;
+    uint32_t it = 0, si = 0;   // pages, ring stages (Q stages and pages)
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        if (p.q_tma) si += 2;   // the segment's Q came through two ring stages
+        const int nb_seq = (s.L + kPage - 1) / kPage;
+        const int tail = s.L & (kPage - 1);
+        const int n = s.hi - s.lo;
+        for (int k = 0; ok && k < n; ++k) {
+            // fewer K steps on a sequence's partly filled last page
+            const int nst = (s.lo + k == nb_seq - 1 && tail != 0) ? (tail + kPvKeys - 1) / kPvKeys : kPvSteps;
+            ok = issue_pv(c, tmem, it + (uint32_t)k, si + (uint32_t)k, k == 0, nst, lane);
+        }
+        if (!ok) break;
+        it += (uint32_t)n;
+        si += (uint32_t)n;
+        if (lane == 0) umma_commit(bar_addr(c, B_OFINAL));
+        __syncwarp();
+    }
+    if (lane == 0) umma_commit(bar_addr(c, B_DRAIN_PV));
+    __syncwarp();
+    drain_bar(c, bar_addr(c, B_DRAIN_PV), 0);
 }
 
 // ----------------------------------------------------------------------------
@@ -610,7 +637,6 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
                               int rb, int hk) {
     const int q = (int)(threadIdx.x >> 5) - 4;
     const int lane = threadIdx.x & 31;
-    const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
     const uint32_t peer = (uint32_t)(cta ^ 1);
@@ -1009,6 +1035,8 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
         mbar_init(bar_addr(c, B_OFINAL), 1);
         mbar_init(bar_addr(c, B_QREADY), 128);
         mbar_init(bar_addr(c, B_DRAIN), 1);
+        mbar_init(bar_addr(c, B_DRAIN_PV), 1);
+        for (int i = 0; i < kSBufs; ++i) mbar_init(bar_addr(c, B_SFREE + i), 1);
         fence_mbar_init();
     }
     if (warp == 8 && lane == 0) {
@@ -1037,8 +1065,10 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
     } else if (warp == 8) {
         const uint64_t pol = gridDim.y > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
         producer_role(c, p, &km128, &km64, &kq, &kqr, rec, cta, rb, hk, pol);
-    } else {
+    } else if (warp == 9) {
         mma_role(c, p, rec, tmem, lane);
+    } else {
+        pv_role(c, p, rec, tmem, lane);
     }
 
     tc_fence_before();
