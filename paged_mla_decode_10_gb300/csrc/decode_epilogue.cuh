@@ -73,9 +73,11 @@ static __device__ __forceinline__ void store_o_half(const DecodeParams &p, uint3
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int j = 16 * sub + 4 * v;
-                    *reinterpret_cast<float4 *>(stage + epi_offset(lane, v)) =
-                        make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                                    __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                    const float2 lo = __fmul2_rn(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                                                 make_float2(inv, inv));
+                    const float2 hi = __fmul2_rn(make_float2(__uint_as_float(o[j + 2]), __uint_as_float(o[j + 3])),
+                                                 make_float2(inv, inv));
+                    *reinterpret_cast<float4 *>(stage + epi_offset(lane, v)) = make_float4(lo.x, lo.y, hi.x, hi.y);
                 }
                 __syncwarp();
 #pragma unroll

@@ -171,16 +171,22 @@ constexpr int kPvKeys = 16;
 constexpr int kPvSteps = kPage / kPvKeys;
 
 // Largest of 64 values by a pairwise tree (depth 6 instead of a 64-long chain).
+// Largest of 64 values (ABS: of their magnitudes) by a tree of three-input maxima:
+// 64 -> 22 -> 8 -> 3 -> 1, 32 instructions at depth 4.
+template <bool ABS>
+__device__ __forceinline__ float max3_step(float a, float b, float c) {
+    return ABS ? fmax3_abs(a, b, c) : fmax3(a, b, c);
+}
+template <bool ABS = false>
 __device__ __forceinline__ float max64(const float (&v)[64]) {
-    float t[32];
+    float t[22], u[8];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) t[i] = fmaxf(v[i], v[i + 32]);
+    for (int i = 0; i < 21; ++i) t[i] = max3_step<ABS>(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    t[21] = max3_step<ABS>(v[63], v[63], v[63]);
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-    }
-    return t[0];
+    for (int i = 0; i < 7; ++i) u[i] = max3_step<ABS>(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[7] = t[21];
+    return max3_step<ABS>(max3_step<ABS>(u[0], u[1], u[2]), max3_step<ABS>(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
 }
 
 // barrier indices
@@ -692,16 +698,16 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
                 }
                 float av[64];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) av[j] = fabsf(__uint_as_float(raw[j]));
-                const float amax = max64(av);
+                for (int j = 0; j < 64; ++j) av[j] = __uint_as_float(raw[j]);
+                const float amax = max64<true>(av);
                 eb = (__float_as_uint(amax) >> 23) & 255u;   // biased exponent E + 127
                 eb = eb < 15u ? 15u : (eb > 254u ? 254u : eb);
                 const float sc = __uint_as_float((268u - eb) << 23) * kXTrim;   // 2^(14-E) (1 - 2^-16)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float t0 = fmaf(__uint_as_float(raw[2 * i]), sc, kXMagic);
-                    const float t1 = fmaf(__uint_as_float(raw[2 * i + 1]), sc, kXMagic);
-                    wd[i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+                    const float2 t = __ffma2_rn(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                                make_float2(sc, sc), make_float2(kXMagic, kXMagic));
+                    wd[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x5410);
                 }
             }
 #endif
@@ -859,8 +865,12 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int j = 8 * ch + 2 * e;
-                        sv[j] = fmaf(__uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5410)) - kXBias, inv, sv[j]);
-                        sv[j + 1] = fmaf(__uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5432)) - kXBias, inv, sv[j + 1]);
+                        const float2 k = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5410)),
+                                                                __uint_as_float(__byte_perm(w4[e], 0x4B00u, 0x5432))),
+                                                    make_float2(-kXBias, -kXBias));
+                        const float2 s2 = __ffma2_rn(k, make_float2(inv, inv), make_float2(sv[j], sv[j + 1]));
+                        sv[j] = s2.x;
+                        sv[j + 1] = s2.y;
                     }
                 }
             }
@@ -889,28 +899,30 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             const float c2 = p.scale_log2;
 #if MLA_F8
             uint32_t pk[16];
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float p0 = ex2_approx(fmaf(sv[4 * j], c2, neg_m));
-                const float p1 = ex2_approx(fmaf(sv[4 * j + 1], c2, neg_m));
-                const float p2 = ex2_approx(fmaf(sv[4 * j + 2], c2, neg_m));
-                const float p3 = ex2_approx(fmaf(sv[4 * j + 3], c2, neg_m));
-                pk[j] = pack_e4m3x4(p0, p1, p2, p3);   // P <= 2^8 (lazy rescale), within e4m3's 448
-                ps[j & 3] += (p0 + p1) + (p2 + p3);    // fp32 terms: the denominator, and so lse, stays exact
+                const float2 a01 = __ffma2_rn(make_float2(sv[4 * j], sv[4 * j + 1]), make_float2(c2, c2), make_float2(neg_m, neg_m));
+                const float2 a23 = __ffma2_rn(make_float2(sv[4 * j + 2], sv[4 * j + 3]), make_float2(c2, c2), make_float2(neg_m, neg_m));
+                const float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
+                const float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+                pk[j] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);   // P <= 2^8 (lazy rescale), within e4m3's 448
+                // fp32 terms: the denominator, and so lse, stays exact
+                ps[0] = __fadd2_rn(ps[0], p01);
+                ps[1] = __fadd2_rn(ps[1], p23);
             }
-            const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            const float psum = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
 #else
             uint32_t pk[32];
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = ex2_approx(fmaf(sv[2 * j], c2, neg_m));
-                const float p1 = ex2_approx(fmaf(sv[2 * j + 1], c2, neg_m));
-                pk[j] = pack_bf16x2(p0, p1);
-                ps[j & 3] += p0 + p1;   // fp32 terms: the denominator, and so lse, stays exact
+                const float2 a = __ffma2_rn(make_float2(sv[2 * j], sv[2 * j + 1]), make_float2(c2, c2), make_float2(neg_m, neg_m));
+                const float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                pk[j] = pack_bf16x2(pp.x, pp.y);
+                ps[j & 1] = __fadd2_rn(ps[j & 1], pp);   // fp32 terms: the denominator, and so lse, stays exact
             }
-            const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            const float psum = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
 #endif
             l_sum += psum;
             // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
@@ -937,7 +949,12 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                     tmem_ld_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+                    for (int j = 0; j < 64; j += 2) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                                                    make_float2(factor, factor));
+                        o[j] = __float_as_uint(v.x);
+                        o[j + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st_32x32b_x64(tmem + lane_base + TM_O + 64u * q4, o);
                 }
             }
