@@ -233,6 +233,7 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
     walk.init(rec);
     Segment s;
     uint32_t it = 0;   // ring stages issued (Q stages and pages)
+    uint32_t first_page = ~0u;
     bool ok = true, first = true;
     // the block's first row, and the row 64 below it, as (head, token) of the query tensor
     const int r0 = rb * kRowsPerBlock;
@@ -267,6 +268,7 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
         } else if (!first) {
             prefetch_q_rows(p, s.b, rb, hk, cta, lane);
         }
+        if (first) first_page = it;   // ring position of the kernel's first page
         first = false;
         for (int base = s.lo; base < s.hi && ok; base += 32) {
             const int n = s.hi - base < 32 ? s.hi - base : 32;
@@ -275,7 +277,11 @@ __device__ void producer_role(const Ctx &c, const DecodeParams &p, const CUtenso
                 const int phys = __shfl_sync(0xffffffffu, mine, k);
                 if (lane == 0) {
                     const uint32_t st = it % kStages;
-                    ok = wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u);
+                    // At the start every SM asks for its query half and pages at once; the
+                    // kernel's second page waits until its first has landed, so that the
+                    // first page and the query are not queued behind the rest.
+                    if (it == first_page + 1u) ok = wait_bar(c, bar_addr(c, B_KFULL + first_page % kStages), 0u);
+                    if (ok) ok = wait_bar(c, bar_addr(c, B_KEMPTY + st), ((it / kStages) & 1u) ^ 1u);
                     if (ok) {
                         const uint32_t full = bar_addr(c, B_KFULL + st);
                         const uint32_t dst = c.base + OFF_K + st * kHalfBytes;
