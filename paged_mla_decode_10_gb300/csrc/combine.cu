@@ -39,12 +39,14 @@ constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 }  // namespace
 
 __global__ void __launch_bounds__(kThreadsCombine, 4) mla_combine_kernel(const __grid_constant__ DecodeParams p) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_g = blockIdx.x * kRowsPerCombineBlock + warp, b = blockIdx.y, hk = blockIdx.z;
-    if (row_g >= p.rows) return;
+    // num_splits comes from the schedule, which completed before the decode kernel began, so it
+    // is read before waiting for the decode; only the partial results need the wait
     const int ns0 = __ldg(p.num_splits + b);
     const int ns = __ldg(p.num_splits + b + 1) - ns0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (row_g >= p.rows) return;
     if (ns == 1) return;   // finished by the decode kernel
     const bool in_range = ns0 >= 0 && ns0 + ns <= p.max_slots;
     const int n = in_range ? ns : 0;
