@@ -815,10 +815,6 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     Segment s;
     uint32_t it = 0, g = 0;
     bool ok = true;
-    // Barrier checks on the softmax warp's chain are probed (test_wait) ahead of the point
-    // where their answer is needed, so that their latency overlaps the arithmetic; the
-    // blocking wait runs only when a probe found the phase still open.
-    bool s_next = false;   // S of the next page already complete (probed at the end of a page)
     while (ok && walk.next(p, s)) {
         int n_vis = p.causal ? s.L - p.s_q + 1 + qi : s.L;
         n_vis = n_vis < 0 ? 0 : (n_vis > s.L ? s.L : n_vis);
@@ -828,11 +824,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             // S/P buffer sb (phase phS); landing slot xb of the peer's tile (phase ph)
             const uint32_t sb = it % kSBufs, phS = (it / kSBufs) & 1u;
             const uint32_t xb = it % kXSlots, ph = (it / kXSlots) & 1u;
-            if (!__all_sync(0xffffffffu, s_next)) {
-                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
-                if (!ok) break;
-            }
-            s_next = false;
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SFULL + sb), phS));
+            if (!ok) break;
             tc_fence_after();
             if (!warp_active) {
                 // rows with no query: P = 0 so that their O rows stay finite
@@ -861,7 +854,6 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             if (!ok) break;
             if ((r & 31) == 0)   // the peer's DMA has landed: its staging buffer it % kXOut is free
                 mbar_arrive_remote_relaxed(it % kXOut ? stagefree_peer[1] : stagefree_peer[0]);
-            const bool s_read = mbar_probe(bar_addr(c, B_SREAD + sb), phS);   // needed before the P store
 #if MLA_XEXACT
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
@@ -942,14 +934,10 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             const float psum = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
 #endif
             l_sum += psum;
-            // the next page's S (buffer (it + 1) % kSBufs), probed now for the loop's next turn
-            s_next = mbar_probe(bar_addr(c, B_SFULL + (it + 1) % kSBufs), ((it + 1) / kSBufs) & 1u);
             // ---- P row -> TMEM, over the S it came from (bf16 pairs, keys along columns),
             // once the exchange warps have copied that S out
-            if (!__all_sync(0xffffffffu, s_read)) {
-                ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), phS));
-                if (!ok) break;
-            }
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_SREAD + sb), phS));
+            if (!ok) break;
             tc_fence_after();
 #if MLA_F8
             tmem_st_32x32b_x16(tmem + lane_base + s_col(sb), pk);

@@ -91,17 +91,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Same, with acquire at cluster scope: for barriers a peer CTA arrives on.
-// Non-blocking check of the same (test_wait returns at once): issued early, its answer is
-// used later, so its latency overlaps other work.
-__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
