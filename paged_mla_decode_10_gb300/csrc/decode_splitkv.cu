@@ -851,12 +851,20 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             if (!ok) break;
             if ((r & 31) == 0)   // the peer's DMA has landed: its staging buffer it % kXOut is free
                 mbar_arrive_remote_relaxed(it % kXOut ? stagefree_peer[1] : stagefree_peer[0]);
+            // One word of every load this lane makes from the landing slot is folded into `fold`,
+            // which the lane stores before the warp barrier that precedes handing the slot back:
+            // a store waits for its data, and a load's words arrive together, so no read of the
+            // slot can still be in flight when the peer's next copy is let in (the arithmetic on
+            // the words may be scheduled after the hand-back, and a load held up behind a long
+            // memory queue would otherwise read the next tile).
+            uint32_t fold = 0u;
 #if MLA_XEXACT
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const float4 t = *reinterpret_cast<const float4 *>(
                     smem_gen + ((xb ? xrow_local[1] : xrow_local[0]) - c.base) + (ch >> 3) * 4096 +
                     (((ch & 7) ^ (r & 7)) << 4));
+                fold ^= __float_as_uint(t.x);
                 sv[4 * ch] += t.x; sv[4 * ch + 1] += t.y; sv[4 * ch + 2] += t.z; sv[4 * ch + 3] += t.w;
             }
 #else
@@ -864,9 +872,11 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 const uint8_t *xr = smem_gen + ((xb ? xrow_local[1] : xrow_local[0]) - c.base);
                 const uint32_t eb = *reinterpret_cast<const uint32_t *>(xr - (r & 31) * 128 + 4096 + (r & 31) * 4);
                 const float inv = __uint_as_float((eb - 14u) << 23) * kXUntrim;   // 2^(E-14) (1 + 2^-16)
+                fold = eb;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint4 t = *reinterpret_cast<const uint4 *>(xr + ((ch ^ (r & 7)) << 4));
+                    fold ^= t.x;
                     const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -881,6 +891,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
                 }
             }
 #endif
+            // the warp's epilogue staging tile is idle until its segment ends
+            *reinterpret_cast<volatile uint32_t *>(smem_gen + OFF_EPI + warp * kEpiWarpBytes + (r & 31) * 4) = fold;
             __syncwarp();
             if ((r & 31) == 0) mbar_arrive_remote_relaxed(xb ? xfree_peer[1] : xfree_peer[0]);
 
