@@ -195,10 +195,13 @@ constexpr int B_KEMPTY = B_KFULL + kStages;
 constexpr int B_SFULL = B_KEMPTY + kStages;
 constexpr int B_SREAD = B_SFULL + kSBufs;       // exchange warps have read S out of TMEM
 constexpr int B_PFULL = B_SREAD + kSBufs;
-constexpr int B_XFULL = B_PFULL + kSBufs;       // peer's partial tile has landed in XIN
-constexpr int B_XINFREE = B_XFULL + 2;          // peer has read the tile we sent into its XIN slot
-constexpr int B_STAGEFREE = B_XINFREE + 2;      // peer has received the tile of an XOUT buffer: reusable
-constexpr int B_PVDONE = B_STAGEFREE + 2;      // kPvBars of them, page i on PVDONE + i % kPvBars
+// Exchange barriers, one per (buffer, warp) at 4 * buffer + warp: a softmax warp and the
+// exchange warp of the same rows deal only with the peer's warps of those rows, so the four
+// row quarters do not wait on one another here.
+constexpr int B_XFULL = B_PFULL + kSBufs;       // peer's tile of the warp's rows has landed in XIN
+constexpr int B_XINFREE = B_XFULL + 8;          // peer has read the tile we sent into its XIN slot
+constexpr int B_STAGEFREE = B_XINFREE + 8;      // peer has received the tile of an XOUT buffer: reusable
+constexpr int B_PVDONE = B_STAGEFREE + 8;      // kPvBars of them, page i on PVDONE + i % kPvBars
 constexpr int B_OFINAL = B_PVDONE + kPvBars;
 constexpr int B_QREADY = B_OFINAL + 1;
 constexpr int B_DRAIN = B_QREADY + 1;             // the QK^T thread's MMAs have completed
@@ -653,7 +656,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     const bool active = rb * kRowsPerBlock + q * 32 < p.rows;
     const uint32_t peer = (uint32_t)(cta ^ 1);
     const uint32_t xin_peer = mapa_shared(c.base + OFF_XIN + (uint32_t)q * kXWarpBytes, peer);
-    const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL), peer), mapa_shared(bar_addr(c, B_XFULL + 1), peer)};
+    const uint32_t xfull_peer[2] = {mapa_shared(bar_addr(c, B_XFULL + q), peer), mapa_shared(bar_addr(c, B_XFULL + 4 + q), peer)};
     // staging layout of a warp's tile: 128-byte row pieces, 16-byte chunks swizzled by row
     uint8_t *half0 = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base)) + OFF_XOUT +
                      (uint32_t)q * kXWarpBytes + (uint32_t)lane * 128u;
@@ -719,7 +722,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
 #endif
             // staged in buffer ob (phase oph), then one DMA per warp tile
             const uint32_t ob = it % kXOut, oph = (it / kXOut) & 1u;
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE + ob), oph ^ 1u));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_STAGEFREE + 4 * (int)ob + q), oph ^ 1u));
             if (!ok) break;
             const uint32_t src = c.base + OFF_XOUT + ob * kXBytes + (uint32_t)q * kXWarpBytes;
             uint8_t *const stg = half0 + ob * kXBytes;   // this lane's row in buffer ob
@@ -731,7 +734,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
                     make_uint4(raw[4 * ch], raw[4 * ch + 1], raw[4 * ch + 2], raw[4 * ch + 3]);
             fence_proxy_async_smem();
             __syncwarp();
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + 4 * (int)b + q), ph ^ 1u));
             if (!ok) break;
             if (lane == 0) bulk_copy_to_peer(dst, src, 4096u, xfull);
 #pragma unroll
@@ -749,7 +752,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
             *reinterpret_cast<uint32_t *>(stg - lane * 128u + 4096u + lane * 4u) = eb;
             fence_proxy_async_smem();
             __syncwarp();
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + b), ph ^ 1u));
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XINFREE + 4 * (int)b + q), ph ^ 1u));
             if (!ok) break;
             if (lane == 0) bulk_copy_to_peer(dst, src, kXWarpBytes, xfull);
 #endif
@@ -777,7 +780,7 @@ __device__ void exchange_role(const Ctx &c, const DecodeParams &p, const int32_t
     // Drain: the last tile sent must have landed before the CTAs may exit.
     if (active) {
         for (uint32_t j = it > (uint32_t)kXOut ? it - kXOut : 0u; j < it; ++j)
-            drain_bar(c, bar_addr(c, B_STAGEFREE + j % kXOut), (j / kXOut) & 1u);
+            drain_bar(c, bar_addr(c, B_STAGEFREE + 4 * (int)(j % kXOut) + q), (j / kXOut) & 1u);
     }
 }
 
@@ -801,10 +804,10 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
     // (fp32: [column half][32 rows][128 B])
     const uint32_t xrow_local[2] = {c.base + OFF_XIN + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u,
                                     c.base + OFF_XIN + kXBytes + (uint32_t)warp * kXWarpBytes + (uint32_t)(r & 31) * 128u};
-    const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE), peer),
-                                    mapa_shared(bar_addr(c, B_XINFREE + 1), peer)};
-    const uint32_t stagefree_peer[2] = {mapa_shared(bar_addr(c, B_STAGEFREE), peer),
-                                        mapa_shared(bar_addr(c, B_STAGEFREE + 1), peer)};
+    const uint32_t xfree_peer[2] = {mapa_shared(bar_addr(c, B_XINFREE + warp), peer),
+                                    mapa_shared(bar_addr(c, B_XINFREE + 4 + warp), peer)};
+    const uint32_t stagefree_peer[2] = {mapa_shared(bar_addr(c, B_STAGEFREE + warp), peer),
+                                        mapa_shared(bar_addr(c, B_STAGEFREE + 4 + warp), peer)};
     uint8_t *smem_gen = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(c.base));
 
     SegmentWalk walk;
@@ -846,8 +849,8 @@ __device__ void softmax_role(const Ctx &c, const DecodeParams &p, const int32_t 
             // ---- the peer's partial logits of the warp's 32 rows: arm XFULL for the
             // warp's tile, wait, add, then tell the peer its staging buffer (and our XIN
             // slot) is free
-            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + xb), kXWarpBytes);
-            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + xb), ph));
+            if ((r & 31) == 0) mbar_arrive_expect_tx(bar_addr(c, B_XFULL + 4 * (int)xb + warp), kXWarpBytes);
+            ok = __all_sync(0xffffffffu, wait_bar(c, bar_addr(c, B_XFULL + 4 * (int)xb + warp), ph));
             if (!ok) break;
             if ((r & 31) == 0)   // the peer's DMA has landed: its staging buffer it % kXOut is free
                 mbar_arrive_remote_relaxed(it % kXOut ? stagefree_peer[1] : stagefree_peer[0]);
@@ -1047,8 +1050,6 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
     const int rb = blockIdx.y, hk = blockIdx.z;
     const int32_t *rec = p.md + part * kMdSize;
 
-    const int rows_here = p.rows - rb * kRowsPerBlock;
-    const int nwa = rows_here >= 128 ? 4 : (rows_here + 31) / 32;   // softmax warps with real rows
 
     if (threadIdx.x == 0) {
         *c.abort_flag = 0;
@@ -1061,11 +1062,11 @@ MLA_SPLITKV_KERNEL(const __grid_constant__ CUtensorMap km128, const __grid_const
             mbar_init(bar_addr(c, B_SREAD + i), 4);
             mbar_init(bar_addr(c, B_PFULL + i), 128);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c, B_XFULL + i), nwa);       // + a warp tile of DMA per arrival
-            mbar_init(bar_addr(c, B_XINFREE + i), nwa);     // remote arrivals from the peer
+        for (int i = 0; i < 8; ++i) {
+            mbar_init(bar_addr(c, B_XFULL + i), 1);       // the softmax warp's arrival + its tile of DMA
+            mbar_init(bar_addr(c, B_XINFREE + i), 1);     // remote arrival from the peer's softmax warp
+            mbar_init(bar_addr(c, B_STAGEFREE + i), 1);   // remote arrival from the peer's softmax warp
         }
-        for (int i = 0; i < 2; ++i) mbar_init(bar_addr(c, B_STAGEFREE + i), nwa);   // remote arrivals from the peer
         for (int i = 0; i < kPvBars; ++i) mbar_init(bar_addr(c, B_PVDONE + i), 1);
         mbar_init(bar_addr(c, B_OFINAL), 1);
         mbar_init(bar_addr(c, B_QREADY), 128);
