@@ -606,11 +606,17 @@ __device__ __forceinline__ bool copy_q_stages(const Ctx &c, uint32_t tmem_q, int
 #if !MLA_F8
             if (h == 1) {
                 // latent dims 128-255: the row as it is into the SW128 Q tile (same
-                // offsets within 1024-byte aligned boxes, so the swizzle carries over)
+                // offsets within 1024-byte aligned boxes, so the swizzle carries over).
+                // Lane m moves chunk j ^ (m & 7) at step j, so that the eight 128-byte rows
+                // of a quarter warp fall on eight different bank groups at every step
+                // (in order, all 32 rows would hit the same four banks).
                 uint4 *dst = reinterpret_cast<uint4 *>(smem_gen + OFF_QL + bx * 16384u + row_in_box);
                 const uint4 *src = reinterpret_cast<const uint4 *>(row);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = src[j];
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t jj = (uint32_t)j ^ (m & 7u);
+                    dst[jj] = src[jj];
+                }
                 continue;
             }
 #endif
@@ -626,8 +632,16 @@ __device__ __forceinline__ bool copy_q_stages(const Ctx &c, uint32_t tmem_q, int
         if ((q >> 1) == h) {
             const uint4 *src = reinterpret_cast<const uint4 *>(stage + kRopeOff + (m & 63u) * kRopeRow);
             uint4 *dst = reinterpret_cast<uint4 *>(smem_gen + OFF_QR + m * kRopeRow);
+            // bf16: two 64-byte rows share a 128-byte bank line; rotating the chunk order by
+            // the row's line index spreads a quarter warp's rows over all 32 banks.  e4m3
+            // (32-byte rows) copies in order: that conflicts only two ways, and the rotated
+            // order measured slower in that build.
+            constexpr uint32_t kCh = kRopeRow / 16, kRowsPerLine = 128u / kRopeRow;
 #pragma unroll
-            for (int k = 0; k < (int)kRopeRow / 16; ++k) dst[k] = src[k];
+            for (uint32_t k = 0; k < kCh; ++k) {
+                const uint32_t kk = MLA_F8 ? k : (k + m / kRowsPerLine) % kCh;
+                dst[kk] = src[kk];
+            }
         }
     }
     tmem_st_wait();
